@@ -1,0 +1,196 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case copies ``oracle/orc.c`` to a temporary directory, plants one
+mistake (a dropped term, a wrong sign, index or order, a transposed operand),
+compiles it with the oracle's own flags, and runs a battery of the pins from
+test_oracle_*.py against it. Every planted mistake must fail at least one pin,
+and the unmodified source must pass them all. Nothing here touches a GPU.
+"""
+import json
+import os
+import shutil
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import exact
+import oracle
+import test_oracle_combine as TC
+import test_oracle_layout as TL
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+SRC = os.path.join(os.path.dirname(oracle.__file__), "orc.c")
+HDR = os.path.join(os.path.dirname(oracle.__file__), "orc.h")
+
+MUTATIONS = {
+    "unfused_multiply_add": ("acc = fmaf(w[ri], r, acc);", "acc = w[ri] * r + acc;"),
+    "descending_k_in_combine": (
+        "        for (int k = 0; k < p->K; ++k) {\n          int64_t ri = route_index(p, s, t, k);\n          if (slot[ri] < 0) continue;",
+        "        for (int k = p->K - 1; k >= 0; --k) {\n          int64_t ri = route_index(p, s, t, k);\n          if (slot[ri] < 0) continue;"),
+    "negative_zero_start": ("float acc = 0.0f;", "float acc = -0.0f;"),
+    "start_not_aligned": ("start[i] = (int32_t)align_up(prev_end, p->alpha);", "start[i] = (int32_t)prev_end;"),
+    "host_counts_raw": ("host_counts[i] = (int32_t)align_up(count[i], p->alpha);", "host_counts[i] = count[i];"),
+    "r_exact_unaligned": ("r_exact[f] = align_up(prev_end, p->alpha);", "r_exact[f] = prev_end;"),
+    "bf16_ties_away": ("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))", "if (dropped >= 0x8000u)"),
+    "bf16_truncate": ("    kept += 1u;\n  return (uint16_t)kept;", "    kept += 0u;\n  return (uint16_t)kept;"),
+    "e4m3_bias_8": ("v = ldexpf((float)(8 + m), e - 7 - 3);", "v = ldexpf((float)(8 + m), e - 8 - 3);"),
+    "e4m3_subnormal_scale": ("v = ldexpf((float)m, -9);", "v = ldexpf((float)m, -10);"),
+    "dup_self_compare": ("for (int j = 0; j < k; ++j)", "for (int j = 0; j <= k; ++j)"),
+    "range_off_by_one": ("if (id < -1 || id >= p->E) return -ORC_ROUTE_RANGE;",
+                         "if (id < -1 || id > p->E) return -ORC_ROUTE_RANGE;"),
+    "row_src_transposed": ("row_src[f * r_stride + row] = (int32_t)ri;",
+                           "row_src[f * r_stride + row] = (int32_t)(((int64_t)t * p->A + s) * p->K + k);"),
+    "row_w_wrong_k": ("row_w[f * r_stride + row] = w[ri];",
+                      "row_w[f * r_stride + row] = w[route_index(p, s, t, (k + 1) % p->K)];"),
+    "tokens_descending": ("    for (int t = 0; t < p->bucket; ++t)\n      for (int k = 0; k < p->K; ++k) {\n        int64_t ri = route_index(p, s, t, k);\n        if (t >= p->T[s]",
+                          "    for (int t = p->bucket - 1; t >= 0; --t)\n      for (int k = 0; k < p->K; ++k) {\n        int64_t ri = route_index(p, s, t, k);\n        if (t >= p->T[s]"),
+    "row_copied_from_wrong_token": ("x + ((int64_t)s * p->bucket + t) * row_bytes",
+                                    "x + ((int64_t)s * p->bucket + (t + 1) % p->T[s]) * row_bytes"),
+    "expert_constant_shifted": ("ldexpf(1.0f, (e % 4) - 1)", "ldexpf(1.0f, (e % 4))"),
+    "fp8_scale_dropped": ("v = v * row_scales[(f * r_stride + r) * nb + h / 128];", "v = v * 1.0f;"),
+    "padding_row_src_zero": ("row_src[f * r_stride + r] = -1;", "row_src[f * r_stride + r] = 0;"),
+}
+
+
+def _pins(orc) -> list:
+    """Runs the battery; returns the names of the pins that failed."""
+    failed = []
+
+    def run(name, fn):
+        try:
+            fn()
+        except AssertionError:
+            failed.append(name)
+
+    def golden_layout():
+        with open(os.path.join(GOLDEN, "ends_convention.json")) as fh:
+            g = json.load(fh)
+        q = g["problem"]
+        p = oracle.Problem(q["A"], q["F"], q["E"], q["K"], q["H"], q["alpha"], q["bucket"],
+                           oracle.BF16, q["T"])
+        ids = np.array(g["ids"], np.int64)
+        r = oracle.round_trip(p, ids, np.ones(ids.shape, np.float32),
+                              np.zeros((1, q["bucket"], q["H"]), np.uint16), orc=orc)
+        for key in ("count", "start", "ends", "host_counts", "r_exact", "slot"):
+            assert np.array_equal(np.asarray(r[key]), np.array(g[key])), key
+        for f, want in enumerate(g["row_src"]):
+            assert r["row_src"][f, : len(want)].tolist() == want
+
+    def random_layout_and_dispatch():
+        rng = np.random.default_rng(21)
+        for trial in range(25):
+            F = int(rng.integers(1, 4)); Ef = int(rng.integers(1, 5)); E = F * Ef
+            K = int(rng.integers(1, min(E, 4) + 1)); A = 2; B = 4
+            a = int(rng.choice([1, 2, 4]))
+            T = [int(rng.integers(1, B + 1)) for _ in range(A)]
+            ids = np.stack([np.stack([rng.permutation(E)[:K] for _ in range(B)]) for _ in range(A)])
+            ids = ids.astype(np.int64)
+            ids[rng.random(ids.shape) < 0.2] = -1
+            w = rng.random((A, B, K)).astype(np.float32)
+            x = rng.integers(0, 1 << 15, size=(A, B, 128)).astype(np.uint16)
+            p = oracle.Problem(A, F, E, K, 128, a, B, oracle.BF16, T)
+            r = oracle.round_trip(p, ids, w, x, orc=orc)
+            TL._check_ends_convention(p, ids, r)
+            TL._check_dispatch(p, ids, w, x, None, r)
+
+    def fp8_dispatch_and_expert():
+        from combine_attention_ffn_gb300 import workloads as W
+        wl = W.named("fp8-2A2F", T=4)
+        inp = W.make_inputs(wl)
+        p = oracle.Problem(wl.A, wl.F, wl.E, wl.K, wl.H, wl.alpha, wl.bucket, oracle.FP8, wl.T)
+        r = oracle.round_trip(p, inp.ids, inp.w, inp.x, inp.x_scales,
+                              expert_mode=oracle.EXPERT_SCALE, orc=orc)
+        TL._check_dispatch(p, inp.ids, inp.w, inp.x, inp.x_scales, r)
+        Ef = wl.E // wl.F
+        for f in range(wl.F):
+            for l in range(Ef):
+                e = f * Ef + l
+                lo, hi = r["start"][f, l], r["ends"][f, l]
+                q = torch.from_numpy(r["rows"][f, lo:hi]).view(torch.float8_e4m3fn).float()
+                sc = torch.from_numpy(r["row_scales"][f, lo:hi]).repeat_interleave(128, dim=1)
+                want = ((q * sc) * 2.0 ** ((e % 4) - 1)).to(torch.bfloat16).view(torch.int16).numpy()
+                assert np.array_equal(r["reply"][f, lo:hi].view(np.int16), want)
+
+    def validate_rules():
+        rng = np.random.default_rng(3)
+        for _ in range(60):
+            ids = rng.integers(-3, 8, size=(2, 5, 3)).astype(np.int64)
+            T = [int(rng.integers(0, 6)) for _ in range(2)]
+            p = oracle.Problem(2, 2, 6, 3, 256, 1, 5, oracle.BF16, T)
+            assert oracle.validate(p, ids, orc) == TL._first_error_numpy(ids, T, 6)
+
+    def combine_exact():
+        rng = np.random.default_rng(4)
+        A, B, K, E, F, H = 2, 2, 5, 12, 3, 128
+        ids = TC._uniform_ids(rng, A, B, K, E)
+        ids[rng.random(ids.shape) < 0.25] = -1
+        ids[1, 1] = -1
+        w = (rng.random((A, B, K)) * 1.7).astype(np.float32)
+        x = TC._rand_bf16(rng, (A, B, H), scale=5.0)
+        p = oracle.Problem(A, F, E, K, H, 4, B, oracle.BF16, [2, 2])
+        r = oracle.round_trip(p, ids, w, x, expert_mode=oracle.EXPERT_SCALE, orc=orc)
+        want = TC._exact_combine(ids, w, x, [2, 2], F, E, lambda e: Fraction(2) ** ((e % 4) - 1))
+        assert np.array_equal(r["out"], want)
+
+    def combine_crafted():
+        w = np.array([[[1.0 + 2.0 ** -8, 16647161 * 2.0 ** -24]]], np.float32)
+        reply = np.zeros((1, 2, 128), np.uint16)
+        reply[0, 0, :] = 0x3F80
+        reply[0, 1, :] = 0x3381
+        p = oracle.Problem(1, 1, 2, 2, 128, 1, 1, oracle.BF16, [1])
+        out = oracle.combine(p, np.array([[[0, 1]]], np.int64), w,
+                             np.array([[[0, 1]]], np.int32), 2, reply, orc=orc)
+        assert np.all(out[0, 0] == 0x3F81)
+
+    def bf16_vs_torch():
+        rng = np.random.default_rng(7)
+        bits = rng.integers(0, 1 << 32, size=1 << 16, dtype=np.uint64).astype(np.uint32)
+        ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)], np.float32)
+        f = np.concatenate([ties, bits.view(np.float32)])
+        f = f[np.isfinite(f)]
+        got = orc.float_to_bf16(f)
+        ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, ref)
+
+    def e4m3_vs_torch():
+        codes = np.arange(256, dtype=np.uint8)
+        got = orc.e4m3_to_float(codes)
+        ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+        ok = ~np.isnan(ref)
+        assert np.array_equal(np.isnan(got), ~ok)
+        assert np.array_equal(got[ok], ref[ok])
+
+    for name, fn in [("golden_layout", golden_layout), ("random_layout_dispatch", random_layout_and_dispatch),
+                     ("fp8", fp8_dispatch_and_expert), ("validate", validate_rules),
+                     ("combine_exact", combine_exact), ("combine_crafted", combine_crafted),
+                     ("bf16", bf16_vs_torch), ("e4m3", e4m3_vs_torch)]:
+        run(name, fn)
+    return failed
+
+
+def _build_variant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"{name}: pattern must occur once"
+    d = tmp_path / name
+    d.mkdir()
+    shutil.copy(HDR, d / "orc.h")
+    (d / "orc.c").write_text(src.replace(old, new))
+    lib = d / "liborc.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", str(d), str(d / "orc.c"), "-o", str(lib), "-lm"],
+                   check=True)
+    return oracle.Oracle(str(lib))
+
+
+def test_unmodified_oracle_passes_battery(orc):
+    assert _pins(orc) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTATIONS[name]
+    mutant = _build_variant(tmp_path, name, old, new)
+    failed = _pins(mutant)
+    assert failed, f"mistake '{name}' passed every pin"
