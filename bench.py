@@ -1,0 +1,481 @@
+"""Benchmark: MoE dispatch + combine round trip on one GB300.
+
+One step is one complete exchange: every source dispatches, every worker
+receives and replies (identity expert: the reply is the received rows, as in
+the pages' communication-only numbers), every source collects. The exchange
+is replayed from one CUDA graph; L2 is flushed (a 256 MB write) before every
+timed step, outside the step's events.
+
+Prints ONE JSON line. `value` is microseconds per round trip (lower is
+better). With --gpus N > 1 (torchrun), every rank runs an independent replica
+(the exchange does not shard across GPUs) and the slowest rank's time is
+reported. `--impl reference` times the CPU oracle instead, on this host.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "dispatch+combine µs/round trip; achieved HBM GB/s vs peak (E128 K8 H2048)"
+FALLBACK_HBM_GBS = 6800.0
+PAGES_CONTEXT_US = {  # afdEP-comm design page, "Result" table: 4 x H100 NVLink, communication only
+    ("2A2F", 2048, 1): 20.7, ("2A2F", 2048, 2048): 192.7,
+    ("2A2F-H4096", 4096, 1): 28.4, ("2A2F-H4096", 4096, 2048): 383.2,
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="2A2F")
+    ap.add_argument("--tokens", type=int, default=2048, help="tokens per source")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_bytes(wl, inp) -> dict:
+    """Bytes the exchange must move once (read x, write routed rows, read
+    replies, write out) plus its metadata, per phase and per launch."""
+    valid = 0
+    for s, T in enumerate(wl.T):
+        valid += int((inp.ids[s, :T] >= 0).sum())
+    A, K, H = wl.A, wl.K, wl.H
+    toks = sum(wl.T)
+    R_in = wl.row_bytes + (4 * (H // 128) if wl.dtype == "fp8" else 0)
+    dispatch = toks * R_in + valid * R_in + toks * K * (8 + 4) + valid * (4 + 4) + toks * K * (4 + 8)
+    combine = valid * 2 * H + toks * 2 * H + toks * K * 8
+    return dict(valid=valid, dispatch=dispatch, combine=combine, total=dispatch + combine,
+                payload=toks * R_in + valid * R_in + valid * 2 * H + toks * 2 * H)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
+    source has not changed since (profiles/traffic.txt)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "combine_attention_ffn_gb300", "csrc",
+                       "afd_combine.cu" if kernel == "combine" else "afd_dispatch.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if parts.get("kernel") == kernel and parts.get("source_sha") == sha \
+                    and parts.get("workload") == workload:
+                return float(parts["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ reference arm
+def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1):
+    """Times the oracle's dispatch + combine (identity expert) on this host."""
+    import oracle
+
+    p = oracle.Problem(wl.A, wl.F, wl.E, wl.K, wl.H, wl.alpha, wl.bucket,
+                       oracle.FP8 if wl.dtype == "fp8" else oracle.BF16, list(wl.T))
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < min_reps or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle.validate(p, inp.ids)
+        lay = oracle.layout(p, inp.ids)
+        r_stride = max(1, int(lay["r_exact"].max()))
+        d = oracle.dispatch(p, inp.ids, inp.w, inp.x, inp.x_scales, lay, r_stride)
+        reply = d["rows"].view(np.uint16).reshape(wl.F, r_stride, wl.H)
+        oracle.combine(p, inp.ids, inp.w, d["slot"], r_stride, reply)
+        times.append((time.perf_counter() - t0) * 1e6)
+    return times
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    from combine_attention_ffn_gb300 import workloads as W
+
+    if rank != 0:
+        return 0
+    wl = W.named(args.config, T=args.tokens)
+    inp = W.make_inputs(wl)
+    if wl.dtype == "fp8":
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU arm times BF16 workloads only"}))
+        return 0
+    cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.warmup)  # warm-up
+    steps = cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.steps)
+    value = statistics.mean(steps)
+    ab = algorithmic_bytes(wl, inp)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl),
+        "gbs": round(ab["total"] / (value * 1e-6) / 1e9, 2),
+        "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle"},
+        "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(wl) -> dict:
+    return {"workload": f"{wl.name}: A={wl.A} sources x T={wl.T[0]} tokens, F={wl.F} workers, "
+                        f"E={wl.E}, K={wl.K}, H={wl.H}, {wl.dtype}, alpha={wl.alpha}, "
+                        f"bucket={wl.bucket}, {wl.routing} routing",
+            "A": wl.A, "F": wl.F, "E": wl.E, "K": wl.K, "H": wl.H, "T_per_source": wl.T[0],
+            "bucket": wl.bucket, "expert_alignment": wl.alpha, "routing": wl.routing,
+            "expert": "identity (reply = received rows)",
+            "l2": "flushed before every timed step (256 MB write, outside the step's events)",
+            "execution": "one CUDA graph per round trip"}
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from combine_attention_ffn_gb300 import afd
+    from combine_attention_ffn_gb300 import build as libbuild
+    from combine_attention_ffn_gb300 import workloads as W
+
+    libbuild.build()
+    wl = W.named(args.config, T=args.tokens)
+    if wl.dtype == "fp8":
+        raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
+    inp = W.make_inputs(wl)
+    buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
+
+    xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+          for s, T in enumerate(wl.T)]
+    ids = [torch.from_numpy(inp.ids[s, :T].copy()).to(dev) for s, T in enumerate(wl.T)]
+    ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s, T in enumerate(wl.T)]
+    outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for T in wl.T]
+
+    def exchange(phase_events=None):
+        if phase_events:
+            phase_events[0].record()
+        for s in range(wl.A):
+            buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
+        if phase_events:
+            phase_events[1].record()
+        for f in range(wl.F):
+            r = buf.worker_receive(f, bucket=wl.bucket)
+            buf.worker_reply(f, r.rows, r.receipt)
+        if phase_events:
+            phase_events[2].record()
+        for s in range(wl.A):
+            buf.source_collect(s, out=outs[s])
+        if phase_events:
+            phase_events[3].record()
+
+    # warm up eagerly, then capture one round trip (with phase events inside
+    # the graph when this PyTorch can record them as graph nodes)
+    for _ in range(2):
+        exchange()
+    torch.cuda.synchronize()
+    try:
+        phase = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    except TypeError:
+        phase = None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        exchange(phase)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+
+    # timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    phase_ms = {"dispatch": [], "combine": []}
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        g.replay()
+        ev[i][1].record()
+        if phase is not None:
+            torch.cuda.synchronize()
+            phase_ms["dispatch"].append(phase[0].elapsed_time(phase[1]))
+            phase_ms["combine"].append(phase[2].elapsed_time(phase[3]))
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    ab = algorithmic_bytes(wl, inp)
+    peak, peak_kind = load_peaks()
+    us = ms * 1e3
+    launches_per_step = 2 + (wl.A if wl.F > 1 else 1 + wl.A)
+
+    # dominant kernel: the phase with the larger share; per-launch bytes and time
+    roofline = None
+    if phase is not None and phase_ms["combine"]:
+        d_ms = statistics.mean(phase_ms["dispatch"])
+        c_ms = statistics.mean(phase_ms["combine"])
+        if c_ms >= d_ms:
+            n_launch = wl.A if wl.F > 1 else 1
+            per_launch_s = c_ms / n_launch * 1e-3
+            per_launch_bytes = ab["combine"] / n_launch
+            kname = "combine"
+        else:
+            per_launch_s = d_ms * 1e-3
+            per_launch_bytes = ab["dispatch"]
+            kname = "dispatch (layout + scatter)"
+        achieved = per_launch_bytes / per_launch_s / 1e9
+        traffic = kernel_traffic("combine" if kname == "combine" else "scatter", f"{wl.name}-T{wl.T[0]}")
+        roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "bytes_per_launch": int(per_launch_bytes),
+                    "us_per_launch": round(per_launch_s * 1e6, 2),
+                    "phase_us": {"dispatch": round(d_ms * 1e3, 2), "combine": round(c_ms * 1e3, 2)}}
+
+    # end to end through the public API, host buffers, copies inside the region
+    e2e = None
+    if rank == 0 or ws > 1:
+        e2e = measure_e2e(torch, buf, wl, inp, dev, steps=max(5, args.steps // 2), flush=flush)
+
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = measure_sweep(torch, afd, W, args.config, dev, flush)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        times = cpu_oracle_round_trip_us(wl, inp, args.cpu_seconds)
+        cpu = {"value": round(statistics.median(times), 1), "unit": "us", "cores": 1, "kind": "oracle",
+               "sample": f"{len(times)} full round trips of the same workload "
+                         f"(validate, layout, dispatch, combine; identity expert), single-threaded C"}
+
+    buf.close()
+    if rank == 0:
+        ctx = PAGES_CONTEXT_US.get((args.config, wl.H, wl.T[0]))
+        line = {
+            "metric": METRIC, "value": round(us, 2), "unit": "us", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic", "config": workload_config(wl),
+            "gbs": round(ab["total"] / (us * 1e-6) / 1e9, 1),
+            "hbm_frac_of_peak": round(ab["total"] / (us * 1e-6) / 1e9 / peak, 4),
+            "peak_gbs": peak, "peak_kind": peak_kind,
+            "algorithmic_bytes": ab["total"],
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps,
+            "wall_s": round(wall, 3),
+            "context": ({"pages_4xH100_nvlink_us": ctx,
+                         "note": "multi-GPU communication-only figure from the pages; not this workload"}
+                        if ctx else None),
+            "sweep": sweep,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(torch, buf, wl, inp, dev, steps: int, flush):
+    """Host buffers in, host result out: pinned H2D of x, ids and weights,
+    the four calls, D2H of the outputs, every step."""
+    hx = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).pin_memory() for s, T in enumerate(wl.T)]
+    hid = [torch.from_numpy(inp.ids[s, :T].copy()).pin_memory() for s, T in enumerate(wl.T)]
+    hw = [torch.from_numpy(inp.w[s, :T].copy()).pin_memory() for s, T in enumerate(wl.T)]
+    hout = [torch.empty((T, wl.H), dtype=torch.int16).pin_memory() for T in wl.T]
+    dx = [torch.empty((T, wl.H), dtype=torch.int16, device=dev) for T in wl.T]
+    did = [torch.empty((T, wl.K), dtype=torch.int64, device=dev) for T in wl.T]
+    dw = [torch.empty((T, wl.K), dtype=torch.float32, device=dev) for T in wl.T]
+    dout = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for T in wl.T]
+    h2d = sum(t.numel() * t.element_size() for t in hx + hid + hw)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def step():
+        for s in range(wl.A):
+            dx[s].copy_(hx[s], non_blocking=True)
+            did[s].copy_(hid[s], non_blocking=True)
+            dw[s].copy_(hw[s], non_blocking=True)
+        for s in range(wl.A):
+            buf.source_dispatch(s, dx[s].view(torch.bfloat16), did[s], dw[s], bucket=wl.bucket)
+        for f in range(wl.F):
+            r = buf.worker_receive(f, bucket=wl.bucket)
+            buf.worker_reply(f, r.rows, r.receipt)
+        for s in range(wl.A):
+            buf.source_collect(s, out=dout[s])
+            hout[s].copy_(dout[s].view(torch.int16), non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return {"value": round(statistics.mean(times) * 1e3, 2), "unit": "us",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "eager calls through the binding; pinned host inputs and outputs"}
+
+
+def measure_sweep(torch, afd, W, config, dev, flush):
+    """Graph-replayed round trip at the workload's other token counts
+    (L2 flushed before each replay)."""
+    out = {}
+    table = {"2A2F": (1, 8, 32, 128, 512, 2048), "2A2F-H4096": (1, 128, 2048)}
+    for name, Ts in (("2A2F", table["2A2F"]), ("2A2F-H4096", table["2A2F-H4096"])):
+        for T in Ts:
+            wl = W.named(name, T=T)
+            inp = W.make_inputs(wl)
+            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha)
+            xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+                  for s in range(wl.A)]
+            ids = [torch.from_numpy(inp.ids[s, :T].copy()).to(dev) for s in range(wl.A)]
+            ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s in range(wl.A)]
+            outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(wl.A)]
+
+            def exchange():
+                for s in range(wl.A):
+                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
+                for f in range(wl.F):
+                    r = buf.worker_receive(f, bucket=wl.bucket)
+                    buf.worker_reply(f, r.rows, r.receipt)
+                for s in range(wl.A):
+                    buf.source_collect(s, out=outs[s])
+
+            exchange()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                exchange()
+            for _ in range(3):
+                g.replay()
+            times = []
+            for _ in range(10):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+            del g
+            buf.close()
+            out[f"{name} T={T}"] = round(statistics.median(times), 2)
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,281 @@
+"""Thin Python binding of libafd (include/afd.h) over ctypes.
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current PyTorch stream becomes the call's stream, and the library's device
+memory comes back as zero-copy tensors. Every step of the exchange runs in
+the library's CUDA kernels; there is no fallback. If ``libafd.so`` has not
+been built, :func:`load_library` raises.
+
+The names follow the afdEP-comm "API contract": ``source_dispatch``,
+``worker_receive``, ``worker_reply``, ``source_collect``. On one GPU the
+source and worker ranks are index arguments of one :class:`Buffer`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libafd.so")
+
+OK, ERR_ARG, ERR_STATE, ERR_BUCKET, ERR_RECEIPT = 0, 1, 2, 3, 4
+ERR_ROUTE_RANGE, ERR_ROUTE_DUP, ERR_CUDA, ERR_OOM, ERR_CAPTURING, ERR_UNSUPPORTED = 5, 6, 7, 8, 9, 10
+BF16, FP8_E4M3 = 0, 1
+
+EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_worker_receive",
+           "afd_worker_reply", "afd_source_collect", "afd_get_error", "afd_clear_error",
+           "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
+           "afd_recv_rows_for_bucket", "afd_version")
+
+
+class AfdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_sources", "num_workers", "num_experts", "top_k", "hidden", "capacity",
+        "expert_alignment", "dtype", "num_sms")]
+
+
+class Recv(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_void_p), ("row_scales", ctypes.c_void_p),
+                ("weights", ctypes.c_void_p), ("row_src", ctypes.c_void_p),
+                ("ends", ctypes.c_void_p), ("host_counts", ctypes.c_void_p),
+                ("num_rows", ctypes.c_int64), ("receipt", ctypes.c_uint64)]
+
+
+class View(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
+                ("num_tokens", ctypes.c_int32), ("is_view", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads libafd.so (once). Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise AfdError(ERR_UNSUPPORTED, f"{p} is missing; build it with "
+                       "`python -m combine_attention_ffn_gb300.build`")
+    lib = ctypes.CDLL(p)
+    v, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+    P = ctypes.POINTER
+    sigs = {
+        "afd_create": (i32, [P(Config), i32, P(v)]),
+        "afd_destroy": (i32, [v]),
+        "afd_source_dispatch": (i32, [v, i32, v, v, v, v, i64, i64, i32, i32, i32, v]),
+        "afd_worker_receive": (i32, [v, i32, i32, i32, v, P(Recv)]),
+        "afd_worker_reply": (i32, [v, i32, v, i64, u64, v]),
+        "afd_source_collect": (i32, [v, i32, v, i32, v, P(View)]),
+        "afd_get_error": (i32, [v, P(i32), P(i32), P(i32), P(i32)]),
+        "afd_clear_error": (i32, [v, v]),
+        "afd_reset_exchange": (i32, [v]),
+        "afd_status_string": (ctypes.c_char_p, [i32]),
+        "afd_error_detail": (ctypes.c_char_p, [v]),
+        "afd_arena_rows": (i64, [v]),
+        "afd_recv_rows_for_bucket": (i64, [v, i32]),
+        "afd_version": (i32, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class _DeviceArray:
+    """Exposes library-owned device memory through __cuda_array_interface__;
+    the tensor made from it keeps the owning Buffer alive."""
+
+    def __init__(self, ptr: int, shape, typestr: str, owner):
+        self.__cuda_array_interface__ = {"shape": tuple(int(s) for s in shape), "typestr": typestr,
+                                         "data": (int(ptr or 0), False), "version": 2,
+                                         "strides": None}
+        self._owner = owner
+
+
+def _wrap(ptr, shape, dtype: torch.dtype, owner, device) -> torch.Tensor:
+    base = {torch.int32: "<i4", torch.float32: "<f4", torch.bfloat16: "<i2",
+            torch.float8_e4m3fn: "|u1", torch.uint8: "|u1"}[dtype]
+    t = torch.as_tensor(_DeviceArray(ptr, shape, base, owner), device=device)
+    if dtype == torch.bfloat16:
+        t = t.view(torch.bfloat16)
+    elif dtype == torch.float8_e4m3fn:
+        t = t.view(torch.float8_e4m3fn)
+    return t
+
+
+def _stream_handle(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+@dataclass
+class Receive:
+    """One worker's received rows (zero-copy views of the context's arena)."""
+    rows: torch.Tensor                 # [num_rows, H] bf16 or float8_e4m3fn
+    row_scales: Optional[torch.Tensor]  # [num_rows, H/128] f32 (FP8)
+    weights: torch.Tensor              # [num_rows] f32
+    row_src: torch.Tensor              # [num_rows] i32
+    ends: torch.Tensor                 # [E/F] i32 on the device
+    host_counts: Optional[np.ndarray]  # [E/F] aligned counts (read_host_counts)
+    num_rows: int
+    receipt: int
+
+
+class Buffer:
+    """One context: A sources and F workers exchanging through this GPU's HBM."""
+
+    def __init__(self, num_sources: int, num_workers: int, num_experts: int, top_k: int,
+                 hidden: int, capacity: int, expert_alignment: int = 1, dtype: str = "bf16",
+                 num_sms: int = 0, device=None):
+        self._lib = load_library()
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None
+                                   else torch.device(device).index or 0)
+        self.cfg = Config(num_sources, num_workers, num_experts, top_k, hidden, capacity,
+                          expert_alignment, FP8_E4M3 if dtype == "fp8" else BF16, num_sms)
+        self.dtype = dtype
+        self.A, self.F, self.E, self.K, self.H = num_sources, num_workers, num_experts, top_k, hidden
+        self.Ef = num_experts // max(num_workers, 1)
+        self.capacity, self.alpha = capacity, expert_alignment
+        h = ctypes.c_void_p()
+        st = self._lib.afd_create(ctypes.byref(self.cfg), self.device.index, ctypes.byref(h))
+        if st != OK:
+            raise AfdError(st, "afd_create: " + self._lib.afd_status_string(st).decode())
+        self._h = h
+        self._outs = {}
+
+    # -- helpers ------------------------------------------------------------
+    def _check(self, st: int, what: str):
+        if st != OK:
+            detail = self._lib.afd_error_detail(self._h).decode() if self._h else ""
+            raise AfdError(st, f"{what}: {self._lib.afd_status_string(st).decode()}: {detail}")
+
+    @property
+    def handle(self) -> int:
+        return int(self._h.value or 0)
+
+    def arena_rows(self) -> int:
+        return int(self._lib.afd_arena_rows(self._h))
+
+    def recv_rows_for_bucket(self, bucket: int) -> int:
+        return int(self._lib.afd_recv_rows_for_bucket(self._h, bucket))
+
+    # -- the four calls -------------------------------------------------------
+    def source_dispatch(self, source: int, x: torch.Tensor, ids: torch.Tensor,
+                        weights: torch.Tensor, x_scale: Optional[torch.Tensor] = None, *,
+                        bucket: int, read_host_counts: bool = False, stream=None) -> None:
+        T = int(x.shape[0]) if x is not None else 0
+        if T:
+            want = torch.float8_e4m3fn if self.dtype == "fp8" else torch.bfloat16
+            if x.dtype != want or tuple(x.shape) != (T, self.H) or not x.is_contiguous():
+                raise AfdError(ERR_ARG, f"x must be contiguous {want} [T, {self.H}]")
+            if ids.dtype != torch.int64 or tuple(ids.shape) != (T, self.K) or not ids.is_contiguous():
+                raise AfdError(ERR_ARG, f"ids must be contiguous int64 [T, {self.K}]")
+            if weights.dtype != torch.float32 or tuple(weights.shape) != (T, self.K) \
+                    or not weights.is_contiguous():
+                raise AfdError(ERR_ARG, f"weights must be contiguous float32 [T, {self.K}]")
+        sst = ssb = 0
+        if x_scale is not None:
+            if x_scale.dtype != torch.float32 or tuple(x_scale.shape) != (T, self.H // 128):
+                raise AfdError(ERR_ARG, f"x_scale must be float32 [T, {self.H // 128}]")
+            sst, ssb = x_scale.stride()
+        st = self._lib.afd_source_dispatch(self._h, source, _ptr(x) if T else None,
+                                           _ptr(ids) if T else None, _ptr(weights) if T else None,
+                                           _ptr(x_scale) if T else None, sst, ssb, T, bucket,
+                                           int(bool(read_host_counts)),
+                                           _stream_handle(stream, self.device))
+        self._check(st, "source_dispatch")
+
+    def worker_receive(self, worker: int, *, bucket: int, read_host_counts: bool = False,
+                       stream=None) -> Receive:
+        r = Recv()
+        st = self._lib.afd_worker_receive(self._h, worker, bucket, int(bool(read_host_counts)),
+                                          _stream_handle(stream, self.device), ctypes.byref(r))
+        self._check(st, "worker_receive")
+        n = int(r.num_rows)
+        rows_dtype = torch.float8_e4m3fn if self.dtype == "fp8" else torch.bfloat16
+        hc = None
+        if r.host_counts:
+            hc = np.ctypeslib.as_array(ctypes.cast(r.host_counts, ctypes.POINTER(ctypes.c_int32)),
+                                       shape=(self.Ef,)).copy()
+        return Receive(
+            rows=_wrap(r.rows, (n, self.H), rows_dtype, self, self.device),
+            row_scales=(_wrap(r.row_scales, (n, self.H // 128), torch.float32, self, self.device)
+                        if r.row_scales else None),
+            weights=_wrap(r.weights, (n,), torch.float32, self, self.device),
+            row_src=_wrap(r.row_src, (n,), torch.int32, self, self.device),
+            ends=_wrap(r.ends, (self.Ef,), torch.int32, self, self.device),
+            host_counts=hc, num_rows=n, receipt=int(r.receipt))
+
+    def worker_reply(self, worker: int, rows: torch.Tensor, receipt: int, stream=None) -> None:
+        if rows.dtype != torch.bfloat16 or rows.dim() != 2 or rows.shape[1] != self.H \
+                or not rows.is_contiguous():
+            raise AfdError(ERR_ARG, f"reply rows must be contiguous bfloat16 [rows, {self.H}]")
+        st = self._lib.afd_worker_reply(self._h, worker, _ptr(rows), int(rows.shape[0]),
+                                        ctypes.c_uint64(receipt), _stream_handle(stream, self.device))
+        self._check(st, "worker_reply")
+
+    def source_collect(self, source: int, *, view: bool = False, out: Optional[torch.Tensor] = None,
+                       num_tokens: Optional[int] = None, stream=None) -> torch.Tensor:
+        """BF16 [T, H]. With view=True and one worker, a read-only view of the
+        context's inbox (valid until the next source_dispatch)."""
+        v = View()
+        if out is None and not (view and self.F == 1):
+            if num_tokens is None:
+                raise AfdError(ERR_ARG, "pass out= or num_tokens=")
+            out = torch.empty((num_tokens, self.H), dtype=torch.bfloat16, device=self.device)
+        st = self._lib.afd_source_collect(self._h, source, _ptr(out), int(bool(view)),
+                                          _stream_handle(stream, self.device), ctypes.byref(v))
+        self._check(st, "source_collect")
+        if v.is_view:
+            T = int(v.num_tokens)
+            base = _wrap(v.data, (max(T, 1) if T else 0, int(v.row_stride)), torch.bfloat16, self,
+                         self.device)
+            return base[:T, : self.H]
+        return out
+
+    # -- errors and lifetime ---------------------------------------------------
+    def get_error(self):
+        c, s, t, k = (ctypes.c_int32() for _ in range(4))
+        st = self._lib.afd_get_error(self._h, ctypes.byref(c), ctypes.byref(s), ctypes.byref(t),
+                                     ctypes.byref(k))
+        self._check(st, "get_error")
+        return c.value, s.value, t.value, k.value
+
+    def clear_error(self, stream=None) -> None:
+        self._check(self._lib.afd_clear_error(self._h, _stream_handle(stream, self.device)),
+                    "clear_error")
+
+    def reset_exchange(self) -> None:
+        self._check(self._lib.afd_reset_exchange(self._h), "reset_exchange")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            st = self._lib.afd_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            if st != OK:
+                raise AfdError(st, "afd_destroy failed")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

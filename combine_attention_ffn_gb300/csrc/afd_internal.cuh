@@ -1,0 +1,99 @@
+// Internal declarations shared by the libafd translation units: launch
+// parameter blocks and the kernel launchers. Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace afd {
+
+constexpr int kMaxSources = 64;
+constexpr int kMaxWorkers = 64;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kChunk = 256;          // tokens per layout chunk = threads per layout block
+constexpr int kChunkWarps = kChunk / 32;
+constexpr int kWorkerShift = 24;     // receipt route code = (worker << 24) | row
+constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
+constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
+static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
+
+constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
+constexpr int kErrDup = 6;    // AFD_ERR_ROUTE_DUP
+constexpr unsigned long long kNoError = ~0ull;
+
+// The sticky route error: the smallest key wins, so the reported route is the
+// first in (source, token, k) order. key = s << 56 | t << 16 | k << 8 | code.
+__host__ __device__ inline unsigned long long route_error_key(int s, int t, int k, int code) {
+  return ((unsigned long long)s << 56) | ((unsigned long long)(uint32_t)t << 16) |
+         ((unsigned long long)k << 8) | (unsigned long long)code;
+}
+
+struct SourceDesc {
+  const uint8_t* x;      // [T][row_bytes]
+  const int64_t* ids;    // [T][K]
+  const float* w;        // [T][K]
+  const float* scale;    // FP8: scale(t, b) = scale[t * sst + b * ssb]
+  int64_t sst, ssb;
+  int32_t T;             // live tokens
+  int32_t tok_off;       // first flattened token of this source
+  int32_t chunk_off;     // first layout chunk of this source
+  int32_t pad_;
+};
+
+// Everything the layout and scatter kernels of one exchange read or write.
+struct DispatchParams {
+  SourceDesc src[kMaxSources];
+  int32_t A, F, E, Ef, K, alpha, bucket;
+  int32_t row_bytes;     // 2H (BF16) or H (FP8)
+  int32_t nscale;        // H / 128 for FP8, else 0
+  int32_t total_tokens;  // sum of T
+  int32_t total_chunks;  // sum of ceil(T / kChunk)
+  int64_t R_arena;       // rows per worker arena
+  // context scratch
+  int32_t* route_tmp;    // [total_tokens][K]: (expert << 8 | rank in chunk) or -1
+  int32_t* chunk_counts; // [total_chunks][E]
+  int32_t* chunk_start;  // [total_chunks][E]: first row of the chunk's run of expert e
+  unsigned int* done;    // last-block counter (returns to 0 after each launch)
+  unsigned long long* err;
+  // context outputs
+  int32_t* starts;       // [E] aligned start of each expert (worker-local rows)
+  int32_t* ends;         // [E] ends[] (worker-local)
+  int32_t* hcounts;      // [E] aligned counts
+  int2* routes;          // receipt [total_tokens][K]: {code, weight bits}
+  int32_t* row_src;      // [F][R_arena]
+  float* row_w;          // [F][R_arena]
+  uint8_t* rows;         // [F][R_arena][row_bytes]
+  float* row_scales;     // [F][R_arena][nscale]
+};
+
+struct CombineParams {
+  const int2* routes[kMaxSources];   // receipt rows of each source, [T][K]
+  uint16_t* out[kMaxSources];        // BF16 [T][out_stride]
+  int64_t out_stride[kMaxSources];   // elements
+  int32_t tok_off[kMaxSources];      // first flattened token of each source in this launch
+  const uint16_t* reply[kMaxWorkers];// BF16 [rows][H] per worker
+  int32_t A, K, H, total_tokens;
+};
+
+struct CopyParams {
+  const uint16_t* src;
+  uint16_t* dst;
+  int64_t src_stride, dst_stride;  // elements
+  int32_t rows, H;
+};
+
+struct LaunchShape {
+  int grid;
+  int block;
+  size_t smem;
+};
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_layout(const DispatchParams& p, int sm_cap, cudaStream_t stream);
+cudaError_t launch_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
+cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
+cudaError_t configure_kernels(int max_experts);
+
+}  // namespace afd

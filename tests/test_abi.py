@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/afd.h declares. No compute calls: these run without a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "afd.h")
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from combine_attention_ffn_gb300 import build
+
+    return build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^AFD_API\s+[\w\s\*]+?\b(afd_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("afd_source_dispatch", "afd_worker_receive", "afd_worker_reply", "afd_source_collect",
+              "afd_create", "afd_destroy", "afd_get_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (afd_\w+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+    lib = ctypes.CDLL(lib_path)
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_signatures_cover_the_header(lib_path):
+    from combine_attention_ffn_gb300 import afd
+
+    assert set(afd.EXPORTS) == set(declared_functions())
+    lib = afd.load_library(lib_path)
+    assert lib.afd_version() >> 16 == 0
+
+
+def test_status_strings_and_no_device(lib_path):
+    from combine_attention_ffn_gb300 import afd
+    import torch
+
+    lib = afd.load_library(lib_path)
+    assert lib.afd_status_string(0) == b"ok"
+    assert b"receipt" in lib.afd_status_string(afd.ERR_RECEIPT)
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the no-device path is not reachable")
+    cfg = afd.Config(2, 2, 8, 2, 256, 16, 1, 0, 0)
+    h = ctypes.c_void_p()
+    st = lib.afd_create(ctypes.byref(cfg), 0, ctypes.byref(h))
+    assert st == afd.ERR_CUDA and not h.value
+
+
+def test_bad_configs_rejected_before_any_device_work(lib_path):
+    from combine_attention_ffn_gb300 import afd
+
+    lib = afd.load_library(lib_path)
+    bad = [
+        afd.Config(2, 3, 8, 2, 256, 16, 1, 0, 0),     # E not a multiple of F
+        afd.Config(2, 2, 8, 9, 256, 16, 1, 0, 0),     # K > E
+        afd.Config(2, 2, 64, 33, 256, 16, 1, 0, 0),   # K > 32
+        afd.Config(2, 2, 8, 2, 200, 16, 1, 0, 0),     # H not a multiple of 256
+        afd.Config(2, 2, 8, 2, 256, 16, 0, 0, 0),     # alignment 0
+        afd.Config(0, 2, 8, 2, 256, 16, 1, 0, 0),     # no sources
+        afd.Config(2, 2, 8, 2, 256, 16, 1, 7, 0),     # unknown dtype
+        afd.Config(2, 2, 2048, 2, 256, 16, 1, 0, 0),  # E above this build's limit
+    ]
+    for cfg in bad:
+        h = ctypes.c_void_p()
+        st = lib.afd_create(ctypes.byref(cfg), 0, ctypes.byref(h))
+        assert st in (afd.ERR_ARG, afd.ERR_UNSUPPORTED), (cfg.num_experts, st)
+        assert not h.value
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from combine_attention_ffn_gb300 import afd
+
+    with pytest.raises(afd.AfdError):
+        afd.load_library(str(tmp_path / "libafd.so"))
