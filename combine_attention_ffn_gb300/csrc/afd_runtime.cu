@@ -316,7 +316,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->err, 0xff, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->row_src, 0xff, (size_t)(F * c->R_arena) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->row_w, 0, (size_t)(F * c->R_arena) * sizeof(float));
-  if (e == cudaSuccess) e = afd::configure_kernels(g.num_experts);
+  if (e == cudaSuccess) e = afd::configure_kernels(afd::kMaxExperts);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     fprintf(stderr, "afd_create: %s\n", cudaGetErrorString(e));
