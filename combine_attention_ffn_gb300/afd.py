@@ -96,9 +96,27 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     return lib
 
 
+class _Context:
+    """Owns one afd_ctx. It is destroyed when the Buffer is closed and no
+    tensor that views the context's memory is alive any more, so a view can
+    never outlive the memory it points at."""
+
+    def __init__(self, lib, handle: ctypes.c_void_p):
+        self.lib = lib
+        self.handle = handle
+
+    def __del__(self):
+        try:
+            if self.handle is not None and self.handle.value:
+                self.lib.afd_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
 class _DeviceArray:
     """Exposes library-owned device memory through __cuda_array_interface__;
-    the tensor made from it keeps the owning Buffer alive."""
+    the tensor made from it keeps the owning context alive."""
 
     def __init__(self, ptr: int, shape, typestr: str, owner):
         self.__cuda_array_interface__ = {"shape": tuple(int(s) for s in shape), "typestr": typestr,
@@ -159,8 +177,8 @@ class Buffer:
         st = self._lib.afd_create(ctypes.byref(self.cfg), self.device.index, ctypes.byref(h))
         if st != OK:
             raise AfdError(st, "afd_create: " + self._lib.afd_status_string(st).decode())
+        self._ctx = _Context(self._lib, h)
         self._h = h
-        self._outs = {}
 
     # -- helpers ------------------------------------------------------------
     def _check(self, st: int, what: str):
@@ -217,12 +235,12 @@ class Buffer:
             hc = np.ctypeslib.as_array(ctypes.cast(r.host_counts, ctypes.POINTER(ctypes.c_int32)),
                                        shape=(self.Ef,)).copy()
         return Receive(
-            rows=_wrap(r.rows, (n, self.H), rows_dtype, self, self.device),
-            row_scales=(_wrap(r.row_scales, (n, self.H // 128), torch.float32, self, self.device)
+            rows=_wrap(r.rows, (n, self.H), rows_dtype, self._ctx, self.device),
+            row_scales=(_wrap(r.row_scales, (n, self.H // 128), torch.float32, self._ctx, self.device)
                         if r.row_scales else None),
-            weights=_wrap(r.weights, (n,), torch.float32, self, self.device),
-            row_src=_wrap(r.row_src, (n,), torch.int32, self, self.device),
-            ends=_wrap(r.ends, (self.Ef,), torch.int32, self, self.device),
+            weights=_wrap(r.weights, (n,), torch.float32, self._ctx, self.device),
+            row_src=_wrap(r.row_src, (n,), torch.int32, self._ctx, self.device),
+            ends=_wrap(r.ends, (self.Ef,), torch.int32, self._ctx, self.device),
             host_counts=hc, num_rows=n, receipt=int(r.receipt))
 
     def worker_reply(self, worker: int, rows: torch.Tensor, receipt: int, stream=None) -> None:
@@ -247,9 +265,8 @@ class Buffer:
         self._check(st, "source_collect")
         if v.is_view:
             T = int(v.num_tokens)
-            base = _wrap(v.data, (max(T, 1) if T else 0, int(v.row_stride)), torch.bfloat16, self,
-                         self.device)
-            return base[:T, : self.H]
+            base = _wrap(v.data, (T, int(v.row_stride)), torch.bfloat16, self._ctx, self.device)
+            return base[:, : self.H]
         return out
 
     # -- errors and lifetime ---------------------------------------------------
@@ -268,14 +285,7 @@ class Buffer:
         self._check(self._lib.afd_reset_exchange(self._h), "reset_exchange")
 
     def close(self) -> None:
-        if getattr(self, "_h", None) is not None and self._h.value:
-            st = self._lib.afd_destroy(self._h)
-            self._h = ctypes.c_void_p()
-            if st != OK:
-                raise AfdError(st, "afd_destroy failed")
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
+        """Releases the context. Its memory is freed (after the device work
+        completes) once no tensor viewing it is alive."""
+        self._ctx = None
+        self._h = ctypes.c_void_p()

@@ -134,9 +134,12 @@ def test_host_side_errors_enqueue_nothing():
         short = torch.zeros((r1.num_rows - 1, wl.H), dtype=torch.bfloat16, device="cuda")
         assert _status(lambda: buf.worker_reply(1, short, r1.receipt)) == afd.ERR_RECEIPT
         assert _status(lambda: buf.source_collect(0, num_tokens=16)) == afd.ERR_STATE
-        buf.worker_reply(0, GH.expert_reply(wl, 0, r0, GH.SCALE), r0.receipt)
+        # the reply rows must stay alive until the combine has read them
+        rep0 = GH.expert_reply(wl, 0, r0, GH.SCALE)
+        rep1 = GH.expert_reply(wl, 1, r1, GH.SCALE)
+        buf.worker_reply(0, rep0, r0.receipt)
         assert _status(lambda: buf.worker_reply(0, rows1, r0.receipt)) == afd.ERR_STATE
-        buf.worker_reply(1, GH.expert_reply(wl, 1, r1, GH.SCALE), r1.receipt)
+        buf.worker_reply(1, rep1, r1.receipt)
         out0 = buf.source_collect(0, num_tokens=16)
         assert _status(lambda: buf.source_collect(0, num_tokens=16)) == afd.ERR_STATE
         # a stale receipt from the finished exchange is rejected next time
@@ -148,8 +151,9 @@ def test_host_side_errors_enqueue_nothing():
         buf.source_dispatch(0, d.x[0], d.ids[0], d.w[0], bucket=B)
         buf.source_dispatch(1, d.x[1], d.ids[1], d.w[1], bucket=B)
         r0b = buf.worker_receive(0, bucket=B)
-        assert _status(lambda: buf.worker_reply(0, GH.expert_reply(wl, 0, r0b, GH.SCALE), r0.receipt)) \
-            == afd.ERR_RECEIPT
+        rep0b = GH.expert_reply(wl, 0, r0b, GH.SCALE)
+        assert _status(lambda: buf.worker_reply(0, rep0b, r0.receipt)) == afd.ERR_RECEIPT
+        torch.cuda.synchronize()
         buf.reset_exchange()
     finally:
         buf.close()

@@ -41,7 +41,7 @@ def _roundtrip_check(wl, mode=GH.SCALE, rhc=False, view=False, transposed=False,
         GH.check_layout(wl, snap, exp, rhc, buf)
         GH.check_outputs(wl, results, exp)
         assert buf.get_error()[0] == 0
-        return results
+        return [GH.out_bits(r) for r in results]
     finally:
         if own:
             buf.close()
@@ -82,7 +82,7 @@ def test_single_worker_view_and_copy(name, T):
     res_view = _roundtrip_check(wl, view=True)
     res_copy = _roundtrip_check(wl, view=False)
     for a, b in zip(res_view, res_copy):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert np.array_equal(a, b)
 
 
 def test_view_flag_with_several_workers_returns_ordinary_result():
