@@ -142,7 +142,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons),
+                "window": "1 s of back-to-back replays just before the timed region, and the region"}
 
 
 def dist_env():
@@ -242,6 +243,7 @@ def main():
         raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
     inp = W.make_inputs(wl)
     buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
+    buf_small = sum(wl.T) * wl.K <= 4096  # one-kernel dispatch (see afd_dispatch.cu)
 
     xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
           for s, T in enumerate(wl.T)]
@@ -283,13 +285,20 @@ def main():
         flush.zero_()
         g.replay()
     torch.cuda.synchronize()
+    # The timed region is short next to nvidia-smi's sampling period, so the
+    # sampler also covers one second of back-to-back replays just before it.
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    soak_end = time.perf_counter() + 1.0
+    while time.perf_counter() < soak_end:
+        for _ in range(200):
+            g.replay()
+        torch.cuda.synchronize()
 
     # timed region
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     phase_ms = {"dispatch": [], "combine": []}
-    clocks = ClockSampler(dev.index)
-    clocks.start()
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -318,7 +327,7 @@ def main():
     ab = algorithmic_bytes(wl, inp)
     peak, peak_kind = load_peaks()
     us = ms * 1e3
-    launches_per_step = 2 + (wl.A if wl.F > 1 else 1 + wl.A)
+    launches_per_step = (1 if buf_small else 2) + (wl.A if wl.F > 1 else 1 + wl.A)
 
     # dominant kernel: the phase with the larger share; per-launch bytes and time
     roofline = None

@@ -1,31 +1,32 @@
 // Combine kernel: gathers each token's reply rows and sums them with the
-// routing weights, and the collect copy kernel.
+// routing weights; and the collect copy kernel.
 //
 // What it computes follows the afdEP-comm "API contract" (source_collect:
-// BF16 [T,H] summed over the selected experts in original token order, the
-// routing weight applied exactly once) and the design page's "19. FP8 combine
+// BF16 [T,H] summed over the selected experts in the source's token order,
+// each routing weight applied once) and the design page's "19. FP8 combine
 // replies" (FP32 sum in slot order, one rounding to BF16). Every element is
 //   acc = +0.0f;  for k = 0..K-1 with a valid route: acc = fma(w_k, reply_k, acc)
 //   out = bf16_round_nearest_even(acc)
 // so the result does not depend on the launch shape.
 //
-// Shape: a warp per token. Each lane owns 16-byte slices (8 BF16) of the
-// hidden row; for a group of up to 8 routes it issues all the slice loads
-// first and then the FMAs in ascending k, so up to 8 x kCombineVecs loads per
-// lane are in flight ("10. Single-FFN reduction" of the design page: the
-// reduction over the top-k rows is branch-free across the slices of a row).
+// Work items are (token, segment): a segment is U x 32 consecutive 16-byte
+// slices of the hidden row, one slice per lane per step (8 BF16 each). A
+// warp takes one item at a time, issues the loads of up to 8 routes at once
+// and then their FMAs in ascending k. Splitting a token's row into segments
+// spreads a few tokens over many warps ("R2" of the afdEP-comm design page
+// spreads few-token combines the same way) and balances large batches.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "afd_device.cuh"
 #include "afd_internal.cuh"
 
 namespace afd {
 namespace {
 
-constexpr int kCombineVecs = 2;   // 16-byte slices per lane per step
-constexpr int kGroup = 8;         // routes whose loads are issued together
+constexpr int kGroup = 8;  // routes whose loads are issued together
 
 __device__ __forceinline__ int source_of(const CombineParams& p, int gt) {
   int s = 0;
@@ -47,74 +48,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+template <int U>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // receipts and replies come from earlier kernels
   const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int K = p.K;
-  const int nvec = p.H >> 3;  // 8 BF16 per 16-byte slice
+  const int nseg = (p.H >> 8) / U;  // 32 lanes x 8 BF16 = 256 elements per slice step
+  const int64_t items = (int64_t)p.total_tokens * nseg;
 
-  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
+  for (int64_t it = gwarp; it < items; it += nwarps) {
+    const int gt = (int)(it / nseg);
+    const int seg = (int)(it - (int64_t)gt * nseg);
     const int s = source_of(p, gt);
     const int t = gt - p.tok_off[s];
     int2 r = make_int2(-1, 0);
     if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    const int v0 = seg * 32 * U + lane;
+
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+
+    for (int k0 = 0; k0 < K; k0 += kGroup) {
+      uint4 buf[kGroup][U];
+      float wk[kGroup];
+      bool ok[kGroup];
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const int k = k0 + j;
+        const int c = __shfl_sync(0xffffffffu, r.x, k & 31);
+        wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, k & 31));
+        ok[j] = (k < K) && (c >= 0);
+        if (ok[j]) {
+          const uint4* row = reinterpret_cast<const uint4*>(
+              p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H);
+#pragma unroll
+          for (int u = 0; u < U; ++u) buf[j][u] = ld_once(row + v0 + u * 32);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        if (!ok[j]) continue;
+#pragma unroll
+        for (int u = 0; u < U; ++u) fma8(acc[u], wk[j], buf[j][u]);
+      }
+    }
+
     uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]);
-
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kCombineVecs) {
-      float acc[kCombineVecs][8];
 #pragma unroll
-      for (int u = 0; u < kCombineVecs; ++u)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-
-      for (int k0 = 0; k0 < K; k0 += kGroup) {
-        uint4 buf[kGroup][kCombineVecs];
-        float wk[kGroup];
-        bool ok[kGroup];
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          const int k = k0 + j;
-          const int c = __shfl_sync(0xffffffffu, r.x, k & 31);
-          const float w = __int_as_float(__shfl_sync(0xffffffffu, r.y, k & 31));
-          ok[j] = (k < K) && (c >= 0);
-          wk[j] = w;
-          if (ok[j]) {
-            const uint4* row = reinterpret_cast<const uint4*>(
-                p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H);
-#pragma unroll
-            for (int u = 0; u < kCombineVecs; ++u) {
-              const int v = v0 + u * 32 + lane;
-              if (v < nvec) buf[j][u] = __ldg(row + v);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          if (!ok[j]) continue;
-#pragma unroll
-          for (int u = 0; u < kCombineVecs; ++u)
-            if (v0 + u * 32 + lane < nvec) fma8(acc[u], wk[j], buf[j][u]);
-        }
-      }
-
-#pragma unroll
-      for (int u = 0; u < kCombineVecs; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < nvec) {
-          uint4 o;
-          o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-          o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-          o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-          o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-          out_row[v] = o;
-        }
-      }
+    for (int u = 0; u < U; ++u) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+      o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+      o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+      o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+      out_row[v0 + u * 32] = o;
     }
   }
 }
 
 __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int nvec = p.H >> 3;
   const int64_t total = (int64_t)p.rows * nvec;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -123,19 +123,39 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
     const int v = (int)(i % nvec);
     const uint4* src = reinterpret_cast<const uint4*>(p.src + row * p.src_stride);
     uint4* dst = reinterpret_cast<uint4*>(p.dst + row * p.dst_stride);
-    dst[v] = __ldg(src + v);
+    dst[v] = ld_once(src + v);
   }
+}
+
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel kernel, int64_t grid, cudaStream_t stream, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
 
+// Both kernels start as programmatic dependents of the previous kernel on the
+// stream and wait for it before reading anything.
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
   if (p.total_tokens <= 0) return cudaSuccess;
-  int grid = (p.total_tokens + 7) / 8;
-  const int cap = sm_cap * 8;
+  const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
+  const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
+  // Two slices per item once there is enough work to fill the device twice.
+  const bool wide = (p.H % 512 == 0) && slices >= 2 * cap * 8;
+  const int64_t items = wide ? slices / 2 : slices;
+  int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;
-  combine_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return wide ? launch_pdl(combine_kernel<2>, grid, stream, p)
+              : launch_pdl(combine_kernel<1>, grid, stream, p);
 }
 
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
@@ -144,8 +164,7 @@ cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
   int64_t grid = (total + 255) / 256;
   const int64_t cap = (int64_t)sm_cap * 8;
   if (grid > cap) grid = cap;
-  copy_kernel<<<(int)grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(copy_kernel, grid, stream, p);
 }
 
 }  // namespace afd

@@ -7,26 +7,28 @@
 // first principles" section 3 (count routes per expert, give every route a
 // slot, copy each token's row to every selected expert; section 7: FP8 rows
 // travel with their scales). Unlike the atomic slot counters described there,
-// slots here are assigned by a stable counting sort, so rows inside an expert
+// slots here come from a stable counting sort, so rows inside an expert
 // follow (source, token) order and every run gives the same layout.
 //
-// Layout (one launch): each 256-thread block owns a chunk of 256 tokens of
-// one source, one token per thread. Per warp and expert a shared-memory lane
-// mask collects which of the warp's 32 tokens route to the expert; a route's
-// rank inside the chunk is the count of earlier warps' tokens plus the popcount
-// of earlier lanes in its own mask. A repeated ID shows up as a bit that is
-// already set. The last block to finish (a completion counter, no waiting)
-// sums the chunk counts per expert, runs the aligned exclusive scan per
-// worker, and turns chunk counts into per-chunk starting rows.
+// Counting: tokens are taken in chunks of 256, one token per thread. For
+// each warp and expert a shared-memory lane mask records which of the warp's
+// 32 tokens route to that expert; a route's rank inside the chunk is the
+// count of earlier warps' tokens plus the popcount of the earlier lanes of
+// its own mask. A repeated ID shows up as a mask bit that is already set.
 //
-// Scatter (one launch): a warp per token reads its route codes, finishes
-// each route's row (chunk start + rank), writes the receipt entries, then
-// reads the source row once with 16-byte loads and stores it to each of the K
-// destination rows.
+// Two paths:
+//  * small exchanges (at most kSmallRoutes routes): one kernel. Every block
+//    counts all routes itself (they are few and sit in L2), scans in shared
+//    memory, then copies its share of the rows. No block waits for another.
+//  * large exchanges: layout_kernel (one block per chunk; the last block to
+//    finish, found with a completion counter, scans the chunk counts) then
+//    scatter_kernel (a warp per token), launched as a programmatic dependent
+//    so that its launch overlaps the layout.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "afd_device.cuh"
 #include "afd_internal.cuh"
 
 namespace afd {
@@ -44,58 +46,196 @@ __device__ __forceinline__ int source_of_token(const DispatchParams& p, int gt) 
   return s;
 }
 
-__device__ __forceinline__ int align_up(int v, int a) { return (v + a - 1) / a * a; }
-
-__device__ __forceinline__ int warp_inclusive_scan(int v) {
-  const int lane = threadIdx.x & 31;
+// Validates the K IDs of token (s, t) held by this thread and marks the valid
+// ones in its warp's lane masks (wmask = this warp's [E] masks). Returns the
+// set of valid routes (bit k). IDs are read as int64 so that a value outside
+// int32 is out of range, not truncated. Errors go to `err` when it is given.
+__device__ __forceinline__ uint32_t mark_token(const int64_t* ids, int K, int E, uint32_t* wmask,
+                                               int lane, int s, int t, unsigned long long* err) {
+  uint32_t valid = 0u;
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    int64_t v[8];
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    int u = __shfl_up_sync(0xffffffffu, v, d);
-    if (lane >= d) v += u;
+    for (int j = 0; j < 8; ++j) v[j] = (k0 + j < K) ? ids[k0 + j] : -1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = k0 + j;
+      const int64_t id = v[j];
+      if (k >= K || id == -1) continue;
+      if (id < -1 || id >= E) {
+        if (err) atomicMin(err, route_error_key(s, t, k, kErrRange));
+        continue;
+      }
+      const uint32_t old = atomicOr(wmask + (int)id, 1u << lane);
+      if (old & (1u << lane)) {  // this token already routed to this expert
+        if (err) atomicMin(err, route_error_key(s, t, k, kErrDup));
+        continue;
+      }
+      valid |= 1u << k;
+    }
   }
-  return v;
+  return valid;
 }
 
-// Sums the chunk counts, runs the aligned scan per worker and writes the
-// per-chunk starting rows. Runs in the last block of the layout launch.
-__device__ void layout_finish(const DispatchParams& p, int32_t* sh_total, int32_t* sh_start) {
-  const int E = p.E, G = p.total_chunks;
+// Per worker: start = exclusive scan of align_up(count, alpha) over its local
+// experts, ends = start + count ("API contract": expert e occupies
+// [align_up(ends[e-1], alpha), ends[e]) with ends[-1] = 0). One warp per
+// worker. Writes sh_start; with `out`, also the global starts/ends/counts.
+__device__ __forceinline__ void worker_scan(const DispatchParams& p, const int32_t* sh_total,
+                                            int32_t* sh_start, bool out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int g = 0; g < G; ++g) run += __ldcg(p.chunk_counts + (int64_t)g * E + e);
-    sh_total[e] = run;
-  }
-  __syncthreads();
-
-  // Per worker: start = exclusive scan of align_up(count, alpha) over its
-  // local experts; ends = start + count ("API contract": expert e occupies
-  // [align_up(ends[e-1], alpha), ends[e]) with ends[-1] = 0).
   for (int f = warp; f < p.F; f += nwarps) {
     int carry = 0;
     for (int l0 = 0; l0 < p.Ef; l0 += 32) {
       const int l = l0 + lane;
       const int e = f * p.Ef + l;
       const int cnt = l < p.Ef ? sh_total[e] : 0;
-      const int al = align_up(cnt, p.alpha);
+      const int al = align_up_dev(cnt, p.alpha);
       const int incl = warp_inclusive_scan(al);
       if (l < p.Ef) {
         const int start = carry + incl - al;
         sh_start[e] = start;
-        p.starts[e] = start;
-        p.ends[e] = start + cnt;
-        p.hcounts[e] = al;
+        if (out) {
+          p.starts[e] = start;
+          p.ends[e] = start + cnt;
+          p.hcounts[e] = al;
+        }
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  __syncthreads();
+}
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = sh_start[e];
-    for (int g = 0; g < G; ++g) {
-      const int c = __ldcg(p.chunk_counts + (int64_t)g * E + e);
+// Padding rows between ends[e] and the next aligned start hold no route:
+// row_src -1, weight +0. One warp per expert, lanes over its padding rows.
+__device__ __forceinline__ void fill_padding(const DispatchParams& p, const int32_t* ends_of) {
+  if (p.alpha <= 1) return;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int e = gwarp; e < p.E; e += nwarps) {
+    const int end = ends_of[e];
+    const int lim = align_up_dev(end, p.alpha);
+    const int64_t base = (int64_t)(e / p.Ef) * p.R_arena;
+    for (int row = end + lane; row < lim; row += 32) {
+      p.row_src[base + row] = -1;
+      p.row_w[base + row] = 0.0f;
+    }
+  }
+}
+
+// A warp copies token (s, t)'s row to each of its routes. `code` is this
+// lane's route (lane < K): (worker << 24) | row, or -1.
+constexpr int kScatterVecs = 8;  // 16-byte vectors per lane in flight
+
+__device__ __forceinline__ void copy_token(const DispatchParams& p, const SourceDesc& src, int t,
+                                           int code) {
+  const int lane = threadIdx.x & 31;
+  const int K = p.K;
+  const int nvec = p.row_bytes >> 4;
+  const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
+    uint4 buf[kScatterVecs];
+#pragma unroll
+    for (int j = 0; j < kScatterVecs; ++j) {
+      const int v = v0 + j * 32 + lane;
+      if (v < nvec) buf[j] = ld_once(xrow + v);
+    }
+    for (int k = 0; k < K; ++k) {
+      const int c = __shfl_sync(0xffffffffu, code, k);
+      if (c < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.rows + ((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.row_bytes);
+#pragma unroll
+      for (int j = 0; j < kScatterVecs; ++j) {
+        const int v = v0 + j * 32 + lane;
+        if (v < nvec) dst[v] = buf[j];
+      }
+    }
+  }
+  // FP8: the row's block scales follow it (read through the caller's strides).
+  for (int b0 = 0; b0 < p.nscale; b0 += 32) {
+    const int b = b0 + lane;
+    float sc = 0.0f;
+    if (b < p.nscale) sc = src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
+    for (int k = 0; k < K; ++k) {
+      const int c = __shfl_sync(0xffffffffu, code, k);
+      if (c < 0 || b >= p.nscale) continue;
+      p.row_scales[((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.nscale + b] = sc;
+    }
+  }
+}
+
+// Writes route (s, t, lane)'s receipt entries for a final row and returns its
+// route code. Called by lanes < K.
+__device__ __forceinline__ int write_route(const DispatchParams& p, int s, int t, int gt, int e,
+                                           int row, float w) {
+  const int f = e / p.Ef;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)f * p.R_arena + row;
+  p.row_src[r] = (s * p.bucket + t) * p.K + lane;
+  p.row_w[r] = w;
+  const int code = (f << kWorkerShift) | row;
+  p.routes[(int64_t)gt * p.K + lane] = make_int2(code, __float_as_int(w));
+  return code;
+}
+
+// ---------------------------------------------------------------- large path
+
+// Sums the chunk counts per expert, scans per worker, and writes each chunk's
+// first row per expert. Runs in the last block of the layout launch; the
+// chunk loop of each expert is split into slices so that loads overlap.
+__device__ void layout_finish(const DispatchParams& p, int32_t* sm) {
+  const int E = p.E, G = p.total_chunks, nthr = blockDim.x;
+  const int P = E <= nthr ? nthr / E : 1;  // slices per expert
+  int32_t* part = sm;                      // [P][E]
+  int32_t* sh_total = part + P * E;        // [E]
+  int32_t* sh_start = sh_total + E;        // [E]
+  const int32_t* cc = p.chunk_counts;
+
+  for (int idx = threadIdx.x; idx < P * E; idx += nthr) {
+    const int e = idx % E, sl = idx / E;
+    const int g0 = (int)((int64_t)G * sl / P), g1 = (int)((int64_t)G * (sl + 1) / P);
+    int sum = 0, g = g0;
+    for (; g + 8 <= g1; g += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(cc + (int64_t)(g + j) * E + e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += v[j];
+    }
+    for (; g < g1; ++g) sum += __ldcg(cc + (int64_t)g * E + e);
+    part[sl * E + e] = sum;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += nthr) {
+    int run = 0;
+    for (int sl = 0; sl < P; ++sl) {
+      const int v = part[sl * E + e];
+      part[sl * E + e] = run;
+      run += v;
+    }
+    sh_total[e] = run;
+  }
+  __syncthreads();
+  worker_scan(p, sh_total, sh_start, true);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < P * E; idx += nthr) {
+    const int e = idx % E, sl = idx / E;
+    const int g0 = (int)((int64_t)G * sl / P), g1 = (int)((int64_t)G * (sl + 1) / P);
+    int run = sh_start[e] + part[sl * E + e], g = g0;
+    for (; g + 8 <= g1; g += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(cc + (int64_t)(g + j) * E + e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        p.chunk_start[(int64_t)(g + j) * E + e] = run;
+        run += v[j];
+      }
+    }
+    for (; g < g1; ++g) {
+      const int c = __ldcg(cc + (int64_t)g * E + e);
       p.chunk_start[(int64_t)g * E + e] = run;
       run += c;
     }
@@ -103,10 +243,11 @@ __device__ void layout_finish(const DispatchParams& p, int32_t* sh_total, int32_
 }
 
 __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ DispatchParams p) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* mask = smem;                                   // [kChunkWarps][E]
-  uint16_t* wbase = reinterpret_cast<uint16_t*>(smem + kChunkWarps * p.E);  // [kChunkWarps][E]
+  extern __shared__ __align__(16) uint32_t smem[];
+  uint32_t* mask = smem;                                                   // [8][E]
+  uint16_t* wbase = reinterpret_cast<uint16_t*>(smem + kChunkWarps * p.E);  // [8][E]
   __shared__ int is_last;
+  pdl_launch_dependents();
 
   const int E = p.E, K = p.K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -120,27 +261,8 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
 
     for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
     __syncthreads();
-
-    // Validate and mark. IDs are read as int64 so that a value outside int32
-    // is caught as out of range rather than truncated.
-    uint32_t valid = 0u;
     const int64_t* ids = src.ids + (int64_t)t * K;
-    if (live) {
-      for (int k = 0; k < K; ++k) {
-        const int64_t id = ids[k];
-        if (id == -1) continue;
-        if (id < -1 || id >= E) {
-          atomicMin(p.err, route_error_key(s, t, k, kErrRange));
-          continue;
-        }
-        const uint32_t old = atomicOr(mask + warp * E + (int)id, 1u << lane);
-        if (old & (1u << lane)) {  // this token already routed to this expert
-          atomicMin(p.err, route_error_key(s, t, k, kErrDup));
-          continue;
-        }
-        valid |= 1u << k;
-      }
-    }
+    const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err) : 0u;
     __syncthreads();
 
     // Warp offsets inside the chunk and the chunk's count per expert.
@@ -177,129 +299,202 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  int32_t* sh_total = reinterpret_cast<int32_t*>(smem);
-  int32_t* sh_start = sh_total + E;
-  layout_finish(p, sh_total, sh_start);
+  layout_finish(p, reinterpret_cast<int32_t*>(smem));
   if (threadIdx.x == 0) *p.done = 0u;
 }
 
-constexpr int kScatterVecs = 8;  // 16-byte vectors per lane in flight
-
 __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ DispatchParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the layout kernel's outputs
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int K = p.K;
-  const int nvec = p.row_bytes >> 4;
 
   for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
     const int s = source_of_token(p, gt);
     const SourceDesc& src = p.src[s];
     const int t = gt - src.tok_off;
-
     int code = -1;
     if (lane < K) {
       const int rt = p.route_tmp[(int64_t)gt * K + lane];
-      const float w = src.w[(int64_t)t * K + lane];
-      float wr = 0.0f;
       if (rt >= 0) {
         const int e = rt >> kRankBits;
         const int rank = rt & ((1 << kRankBits) - 1);
         const int g = src.chunk_off + t / kChunk;
         const int row = p.chunk_start[(int64_t)g * p.E + e] + rank;
-        const int f = e / p.Ef;
-        code = (f << kWorkerShift) | row;
-        const int64_t r = (int64_t)f * p.R_arena + row;
-        p.row_src[r] = (s * p.bucket + t) * K + lane;
-        p.row_w[r] = w;
-        wr = w;
+        code = write_route(p, s, t, gt, e, row, src.w[(int64_t)t * K + lane]);
+      } else {
+        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
       }
-      p.routes[(int64_t)gt * K + lane] = make_int2(code, __float_as_int(wr));
     }
+    copy_token(p, src, t, code);
+  }
+  fill_padding(p, p.ends);
+}
 
-    // Read the row once, write it to every selected expert row.
-    const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
-      uint4 buf[kScatterVecs];
+// ---------------------------------------------------------------- small path
+
+__global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_constant__ DispatchParams p) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  const int E = p.E, K = p.K, N = p.total_tokens;
+  const int G = (N + kChunk - 1) / kChunk;
+  uint32_t* mask = smem;                                   // [8][E]
+  uint32_t* rinfo = mask + kChunkWarps * E;                // [N*K]: (e << 8 | rank) or ~0
+  int32_t* sh_start = reinterpret_cast<int32_t*>(rinfo + N * K);  // [E]
+  int32_t* sh_total = sh_start + E;                        // [E]
+  uint16_t* wbase = reinterpret_cast<uint16_t*>(sh_total + E);    // [8][E]
+  uint16_t* ccnt = wbase + kChunkWarps * E;                // [G][E]
+
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long* err = blockIdx.x == 0 ? p.err : nullptr;
+
+  // Pass 1 (every block, all routes): ranks inside each chunk, chunk counts.
+  for (int c = 0; c < G; ++c) {
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
+    __syncthreads();
+    const int gt = c * kChunk + threadIdx.x;
+    const bool live = gt < N;
+    int s = 0, t = 0;
+    const int64_t* ids = nullptr;
+    uint32_t valid = 0u;
+    if (live) {
+      s = source_of_token(p, gt);
+      t = gt - p.src[s].tok_off;
+      ids = p.src[s].ids + (int64_t)t * K;
+      valid = mark_token(ids, K, E, mask + warp * E, lane, s, t, err);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = 0;
 #pragma unroll
-      for (int j = 0; j < kScatterVecs; ++j) {
-        const int v = v0 + j * 32 + lane;
-        if (v < nvec) buf[j] = __ldg(xrow + v);
+      for (int w = 0; w < kChunkWarps; ++w) {
+        wbase[w * E + e] = (uint16_t)run;
+        run += __popc(mask[w * E + e]);
       }
+      ccnt[c * E + e] = (uint16_t)run;
+    }
+    __syncthreads();
+    if (live) {
+      const uint32_t lanes_before = (1u << lane) - 1u;
       for (int k = 0; k < K; ++k) {
-        const int c = __shfl_sync(0xffffffffu, code, k);
-        if (c < 0) continue;
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.rows + ((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.row_bytes);
-#pragma unroll
-        for (int j = 0; j < kScatterVecs; ++j) {
-          const int v = v0 + j * 32 + lane;
-          if (v < nvec) dst[v] = buf[j];
+        uint32_t info = ~0u;
+        if ((valid >> k) & 1u) {
+          const int e = (int)ids[k];
+          info = ((uint32_t)e << kRankBits) |
+                 (uint32_t)(wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before));
         }
+        rinfo[gt * K + k] = info;
       }
     }
-
-    // FP8: the row's block scales follow it (read through the caller's strides).
-    for (int b0 = 0; b0 < p.nscale; b0 += 32) {
-      const int b = b0 + lane;
-      float sc = 0.0f;
-      if (b < p.nscale) sc = src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
-      for (int k = 0; k < K; ++k) {
-        const int c = __shfl_sync(0xffffffffu, code, k);
-        if (c < 0 || b >= p.nscale) continue;
-        p.row_scales[((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.nscale + b] = sc;
-      }
-    }
+    __syncthreads();
   }
 
-  // Padding rows between ends[e] and the next aligned start: no route, so
-  // row_src -1 and weight +0.
-  if (p.alpha > 1) {
-    const int64_t per = p.alpha - 1;
-    const int64_t items = (int64_t)p.E * per;
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += nthreads) {
-      const int e = (int)(i / per);
-      const int j = (int)(i % per);
-      const int end = p.ends[e];
-      const int row = end + j;
-      if (row < align_up(end, p.alpha)) {
-        const int64_t r = (int64_t)(e / p.Ef) * p.R_arena + row;
-        p.row_src[r] = -1;
-        p.row_w[r] = 0.0f;
+  // Scan: chunk prefixes per expert (in place), totals, aligned starts.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < G; ++c) {
+      const int v = ccnt[c * E + e];
+      ccnt[c * E + e] = (uint16_t)run;
+      run += v;
+    }
+    sh_total[e] = run;
+  }
+  __syncthreads();
+  worker_scan(p, sh_total, sh_start, blockIdx.x == 0);
+  __syncthreads();
+
+  // Pass 2: this block's share of the tokens.
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int gt = gwarp; gt < N; gt += nwarps) {
+    const int s = source_of_token(p, gt);
+    const SourceDesc& src = p.src[s];
+    const int t = gt - src.tok_off;
+    int code = -1;
+    if (lane < K) {
+      const uint32_t info = rinfo[gt * K + lane];
+      if (info != ~0u) {
+        const int e = (int)(info >> kRankBits);
+        const int row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
+        code = write_route(p, s, t, gt, e, row, src.w[(int64_t)t * K + lane]);
+      } else {
+        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
       }
     }
+    copy_token(p, src, t, code);
   }
+
+  // Padding rows, from this block's own copy of the layout.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
+  __syncthreads();
+  fill_padding(p, sh_total);
+}
+
+size_t layout_smem(int E) {
+  const size_t count = (size_t)kChunkWarps * E * (sizeof(uint32_t) + sizeof(uint16_t));
+  const size_t finish = (size_t)(kChunk + 2 * E) * sizeof(int32_t);
+  return count > finish ? count : finish;
+}
+
+size_t small_smem(int E, int N, int K) {
+  const int G = (N + kChunk - 1) / kChunk;
+  return (size_t)kChunkWarps * E * 4 + (size_t)N * K * 4 + (size_t)2 * E * 4 +
+         (size_t)kChunkWarps * E * 2 + (size_t)G * E * 2;
+}
+
+template <typename Kernel>
+cudaError_t launch(Kernel kernel, int grid, int block, size_t smem, cudaStream_t stream, bool pdl,
+                   const DispatchParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
 
-static size_t layout_smem(int E) {
-  return (size_t)kChunkWarps * E * sizeof(uint32_t) + (size_t)kChunkWarps * E * sizeof(uint16_t);
+bool dispatch_is_small(const DispatchParams& p) {
+  return (int64_t)p.total_tokens * p.K <= kSmallRoutes &&
+         small_smem(p.E, p.total_tokens, p.K) <= (size_t)kSmallSmemMax;
 }
 
-cudaError_t configure_kernels(int max_experts) {
-  return cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)layout_smem(max_experts));
+cudaError_t configure_dispatch_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)layout_smem(kMaxExperts));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmallSmemMax);
+  return e;
 }
 
-cudaError_t launch_layout(const DispatchParams& p, int /*sm_cap*/, cudaStream_t stream) {
-  const int grid = p.total_chunks > 0 ? p.total_chunks : 1;
-  layout_kernel<<<grid, kChunk, layout_smem(p.E), stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
+// Launches the exchange's dispatch. The first kernel waits for all earlier
+// work on the stream (a normal launch), so it never overlaps the previous
+// exchange's combine, which still reads the arenas it overwrites.
+cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   const int block = 256;
-  const int warps_needed = p.total_tokens;
-  int grid = (warps_needed + 7) / 8;
-  const int pad_items = p.alpha > 1 ? p.E * (p.alpha - 1) : 0;
-  if (grid < (pad_items + block - 1) / block) grid = (pad_items + block - 1) / block;
-  const int cap = sm_cap * 8;
-  if (grid > cap) grid = cap;
+  if (dispatch_is_small(p)) {
+    int grid = (p.total_tokens + 7) / 8;
+    if (grid > sm_cap) grid = sm_cap;
+    if (grid < 1) grid = 1;
+    return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,
+                  false, p);
+  }
+  const int lgrid = p.total_chunks > 0 ? p.total_chunks : 1;
+  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(p.E), stream, false, p);
+  if (e != cudaSuccess) return e;
+  int grid = (p.total_tokens + 7) / 8;
+  if (grid > sm_cap * 8) grid = sm_cap * 8;
   if (grid < 1) grid = 1;
-  scatter_kernel<<<grid, block, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch(scatter_kernel, grid, block, 0, stream, true, p);
 }
 
 }  // namespace afd

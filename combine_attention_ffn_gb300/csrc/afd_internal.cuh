@@ -16,6 +16,8 @@ constexpr int kChunkWarps = kChunk / 32;
 constexpr int kWorkerShift = 24;     // receipt route code = (worker << 24) | row
 constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
 constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
+constexpr int kSmallRoutes = 4096;   // exchanges up to this many routes take the one-kernel dispatch
+constexpr int kSmallSmemMax = 110 * 1024;
 static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 
 constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
@@ -83,17 +85,11 @@ struct CopyParams {
   int32_t rows, H;
 };
 
-struct LaunchShape {
-  int grid;
-  int block;
-  size_t smem;
-};
-
 // Launchers (return the launch's cudaError_t).
-cudaError_t launch_layout(const DispatchParams& p, int sm_cap, cudaStream_t stream);
-cudaError_t launch_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
+bool dispatch_is_small(const DispatchParams& p);
+cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
-cudaError_t configure_kernels(int max_experts);
+cudaError_t configure_dispatch_kernels();
 
 }  // namespace afd

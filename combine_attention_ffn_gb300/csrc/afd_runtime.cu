@@ -316,7 +316,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->err, 0xff, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->row_src, 0xff, (size_t)(F * c->R_arena) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->row_w, 0, (size_t)(F * c->R_arena) * sizeof(float));
-  if (e == cudaSuccess) e = afd::configure_kernels(afd::kMaxExperts);
+  if (e == cudaSuccess) e = afd::configure_dispatch_kernels();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     fprintf(stderr, "afd_create: %s\n", cudaGetErrorString(e));
@@ -433,10 +433,8 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
     p.row_w = c->row_w;
     p.rows = c->rows;
     p.row_scales = c->row_scales;
-    cudaError_t e = afd::launch_layout(p, c->sm_cap, stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "layout launch");
-    e = afd::launch_scatter(p, c->sm_cap, stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "scatter launch");
+    cudaError_t e = afd::launch_dispatch(p, c->sm_cap, stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "dispatch launch");
     c->phase = kDispatched;
   }
   return mark_stream(c, stream);

@@ -94,8 +94,9 @@ def test_fp8_transposed_scale_view():
     _roundtrip_check(W.named("fp8-2A2F", T=128), transposed=True)
 
 
-def test_sm_cap_gives_identical_results():
-    _roundtrip_check(W.named("2A2F", T=512), num_sms=3)
+@pytest.mark.parametrize("T,sms", [(512, 3), (64, 1), (2048, 7)])
+def test_sm_cap_gives_identical_results(T, sms):
+    _roundtrip_check(W.named("2A2F", T=T), num_sms=sms)
 
 
 def test_crafted_fused_ascending_chain_on_gpu():
@@ -170,6 +171,15 @@ def test_edge_cases():
         W.Workload("k32", A=2, F=4, E=64, K=32, H=256, alpha=2, capacity=96, bucket=96, T=(96, 50)),
         W.Workload("a=5", A=5, F=2, E=32, K=6, H=1024, alpha=16, capacity=200, bucket=160,
                    T=(160, 0, 77, 1, 159)),
+        # the one-kernel dispatch takes up to 4096 routes; both sides of the switch
+        W.Workload("small-max", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
+                   T=(4096,)),
+        W.Workload("large-min", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
+                   T=(4097,)),
+        W.Workload("E1024-small", A=2, F=4, E=1024, K=4, H=256, alpha=8, capacity=600, bucket=600,
+                   T=(512, 500)),
+        W.Workload("E1024-large", A=2, F=4, E=1024, K=4, H=256, alpha=8, capacity=600, bucket=600,
+                   T=(600, 600)),
     ]
     for wl in cases:
         _roundtrip_check(wl, mode=GH.SCALE)
