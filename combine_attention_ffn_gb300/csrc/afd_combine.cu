@@ -112,6 +112,72 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   }
 }
 
+// Large batches, K <= 8: a warp per token. The token's route codes are read
+// once; the hidden row is then walked in 512-byte segments (one 16-byte
+// slice per lane) with a two-stage register pipeline: the loads of segment
+// i+1 (one per route) are in flight while segment i is summed and stored.
+__device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* const (&rowp)[kGroup],
+                                         uint32_t okmask, int v) {
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j)
+    if ((okmask >> j) & 1u) buf[j] = ld_once(reinterpret_cast<const uint4*>(rowp[j]) + v);
+}
+
+__device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGroup],
+                                        const float (&wk)[kGroup], uint32_t okmask, int v) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j)
+    if ((okmask >> j) & 1u) fma8(acc, wk[j], buf[j]);
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  out_row[v] = o;
+}
+
+__global__ void __launch_bounds__(64) combine_token_kernel(const __grid_constant__ CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;
+  const int nseg = p.H >> 8;
+
+  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
+    const int s = source_of(p, gt);
+    const int t = gt - p.tok_off[s];
+    int2 r = make_int2(-1, 0);
+    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    const uint16_t* rowp[kGroup];
+    float wk[kGroup];
+    uint32_t okmask = 0u;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const int c = __shfl_sync(0xffffffffu, r.x, j);
+      wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
+      const bool ok = (j < K) && (c >= 0);
+      okmask |= (ok ? 1u : 0u) << j;
+      rowp[j] = ok ? p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
+    }
+    uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]);
+    uint4 a[kGroup], b[kGroup];
+    load_seg(a, rowp, okmask, lane);
+    int seg = 0;
+    for (; seg + 2 <= nseg; seg += 2) {
+      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane);
+      sum_seg(out_row, a, wk, okmask, seg * 32 + lane);
+      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane);
+      sum_seg(out_row, b, wk, okmask, (seg + 1) * 32 + lane);
+    }
+    if (seg < nseg) sum_seg(out_row, a, wk, okmask, seg * 32 + lane);
+  }
+}
+
 __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -128,10 +194,10 @@ __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyP
 }
 
 template <typename Kernel, typename Params>
-cudaError_t launch_pdl(Kernel kernel, int64_t grid, cudaStream_t stream, const Params& p) {
+cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stream, const Params& p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(block);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -147,6 +213,13 @@ cudaError_t launch_pdl(Kernel kernel, int64_t grid, cudaStream_t stream, const P
 // stream and wait for it before reading anything.
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
   if (p.total_tokens <= 0) return cudaSuccess;
+  if (p.K <= kGroup && p.total_tokens >= sm_cap * 8) {
+    // enough tokens for a warp each on every SM: the pipelined per-token
+    // kernel, in two-warp blocks so that tokens spread evenly over the SMs
+    int64_t grid = (p.total_tokens + 1) / 2;
+    if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
+    return launch_pdl(combine_token_kernel, grid, 64, stream, p);
+  }
   const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
   const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
   // Two slices per item once there is enough work to fill the device twice.
@@ -154,8 +227,8 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
   const int64_t items = wide ? slices / 2 : slices;
   int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;
-  return wide ? launch_pdl(combine_kernel<2>, grid, stream, p)
-              : launch_pdl(combine_kernel<1>, grid, stream, p);
+  return wide ? launch_pdl(combine_kernel<2>, grid, 256, stream, p)
+              : launch_pdl(combine_kernel<1>, grid, 256, stream, p);
 }
 
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
@@ -164,7 +237,7 @@ cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
   int64_t grid = (total + 255) / 256;
   const int64_t cap = (int64_t)sm_cap * 8;
   if (grid > cap) grid = cap;
-  return launch_pdl(copy_kernel, grid, stream, p);
+  return launch_pdl(copy_kernel, grid, 256, stream, p);
 }
 
 }  // namespace afd

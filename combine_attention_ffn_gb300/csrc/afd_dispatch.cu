@@ -20,10 +20,12 @@
 //  * small exchanges (at most kSmallRoutes routes): one kernel. Every block
 //    counts all routes itself (they are few and sit in L2), scans in shared
 //    memory, then copies its share of the rows. No block waits for another.
-//  * large exchanges: layout_kernel (one block per chunk; the last block to
-//    finish, found with a completion counter, scans the chunk counts) then
+//  * large exchanges: layout_kernel (one block per chunk of 256 tokens) then
 //    scatter_kernel (a warp per token), launched as a programmatic dependent
-//    so that its launch overlaps the layout.
+//    so that its launch overlaps the layout. When the chunk x expert counts
+//    are few (at most kBlockScanMax), every scatter block reads them and
+//    scans them in shared memory; otherwise the last layout block to finish
+//    (found with a completion counter; nobody waits) scans them once.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -292,6 +294,8 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
     }
   }
 
+  if (p.block_scan) return;  // every scatter block scans the chunk counts itself
+
   // The last block to arrive finishes the layout; nobody waits.
   __threadfence();
   __syncthreads();
@@ -303,13 +307,44 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
   if (threadIdx.x == 0) *p.done = 0u;
 }
 
-__global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ DispatchParams p) {
+__global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ DispatchParams p) {
+  extern __shared__ __align__(16) int32_t ssm[];
   pdl_launch_dependents();
   pdl_wait();  // the layout kernel's outputs
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K;
+  const int K = p.K, E = p.E, G = p.total_chunks;
+
+  // With few chunk counts, each block turns them into chunk starting rows in
+  // shared memory (one parallel read from L2) instead of waiting for a
+  // separate scan: cstart[g][e], totals, then the aligned starts.
+  int32_t* cstart = ssm;              // [G][E]
+  int32_t* sh_total = cstart + G * E; // [E]
+  int32_t* sh_start = sh_total + E;   // [E]
+  const int32_t* chunk_start = p.chunk_start;
+  const int32_t* ends = p.ends;
+  if (p.block_scan) {
+    for (int i = threadIdx.x; i < G * E; i += blockDim.x) cstart[i] = __ldcg(p.chunk_counts + i);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int g = 0; g < G; ++g) {
+        const int v = cstart[g * E + e];
+        cstart[g * E + e] = run;
+        run += v;
+      }
+      sh_total[e] = run;
+    }
+    __syncthreads();
+    worker_scan(p, sh_total, sh_start, blockIdx.x == 0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * E; i += blockDim.x) cstart[i] += sh_start[i % E];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
+    __syncthreads();
+    chunk_start = cstart;
+    ends = sh_total;
+  }
 
   for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
     const int s = source_of_token(p, gt);
@@ -322,7 +357,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Di
         const int e = rt >> kRankBits;
         const int rank = rt & ((1 << kRankBits) - 1);
         const int g = src.chunk_off + t / kChunk;
-        const int row = p.chunk_start[(int64_t)g * p.E + e] + rank;
+        const int row = chunk_start[g * E + e] + rank;
         code = write_route(p, s, t, gt, e, row, src.w[(int64_t)t * K + lane]);
       } else {
         p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
@@ -330,7 +365,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Di
     }
     copy_token(p, src, t, code);
   }
-  fill_padding(p, p.ends);
+  fill_padding(p, ends);
 }
 
 // ---------------------------------------------------------------- small path
@@ -438,6 +473,8 @@ size_t layout_smem(int E) {
   return count > finish ? count : finish;
 }
 
+size_t scatter_smem(int GE, int E) { return (size_t)(GE + 2 * E) * sizeof(int32_t); }
+
 size_t small_smem(int E, int N, int K) {
   const int G = (N + kChunk - 1) / kChunk;
   return (size_t)kChunkWarps * E * 4 + (size_t)N * K * 4 + (size_t)2 * E * 4 +
@@ -473,6 +510,9 @@ cudaError_t configure_dispatch_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)scatter_smem(kBlockScanMax, kMaxExperts));
   return e;
 }
 
@@ -488,13 +528,17 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
     return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,
                   false, p);
   }
-  const int lgrid = p.total_chunks > 0 ? p.total_chunks : 1;
-  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(p.E), stream, false, p);
+  DispatchParams q = p;
+  q.block_scan = (int64_t)p.total_chunks * p.E <= kBlockScanMax ? 1 : 0;
+  const int lgrid = q.total_chunks > 0 ? q.total_chunks : 1;
+  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(q.E), stream, false, q);
   if (e != cudaSuccess) return e;
-  int grid = (p.total_tokens + 7) / 8;
+  // four warps (tokens) per block, so that blocks spread evenly over the SMs
+  int grid = (q.total_tokens + 3) / 4;
   if (grid > sm_cap * 8) grid = sm_cap * 8;
   if (grid < 1) grid = 1;
-  return launch(scatter_kernel, grid, block, 0, stream, true, p);
+  const size_t smem = q.block_scan ? scatter_smem(q.total_chunks * q.E, q.E) : 0;
+  return launch(scatter_kernel, grid, 128, smem, stream, true, q);
 }
 
 }  // namespace afd

@@ -18,6 +18,7 @@ constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
 constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
 constexpr int kSmallRoutes = 4096;   // exchanges up to this many routes take the one-kernel dispatch
 constexpr int kSmallSmemMax = 110 * 1024;
+constexpr int kBlockScanMax = 8192;  // chunk x expert counts each scatter block scans itself
 static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 
 constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
@@ -52,6 +53,7 @@ struct DispatchParams {
   int32_t total_tokens;  // sum of T
   int32_t total_chunks;  // sum of ceil(T / kChunk)
   int64_t R_arena;       // rows per worker arena
+  int32_t block_scan;    // 1: every scatter block scans the chunk counts itself
   // context scratch
   int32_t* route_tmp;    // [total_tokens][K]: (expert << 8 | rank in chunk) or -1
   int32_t* chunk_counts; // [total_chunks][E]
