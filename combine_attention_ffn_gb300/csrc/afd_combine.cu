@@ -213,7 +213,7 @@ cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stre
 // stream and wait for it before reading anything.
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
   if (p.total_tokens <= 0) return cudaSuccess;
-  if (p.K <= kGroup && p.total_tokens >= sm_cap * 8) {
+  if (p.K <= kGroup && p.total_tokens >= sm_cap * AFD_TOKEN_COMBINE_MIN) {
     // enough tokens for a warp each on every SM: the pipelined per-token
     // kernel, in two-warp blocks so that tokens spread evenly over the SMs
     int64_t grid = (p.total_tokens + 1) / 2;

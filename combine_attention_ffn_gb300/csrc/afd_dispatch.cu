@@ -127,21 +127,35 @@ __device__ __forceinline__ void fill_padding(const DispatchParams& p, const int3
 }
 
 // A warp copies token (s, t)'s row to each of its routes. `code` is this
-// lane's route (lane < K): (worker << 24) | row, or -1.
+// lane's route (lane < K): (worker << 24) | row, or -1. The row is moved in
+// pieces of 32 x kScatterVecs 16-byte vectors; `pre` holds the first piece
+// when the caller loaded it early (have_pre).
 constexpr int kScatterVecs = 8;  // 16-byte vectors per lane in flight
 
+__device__ __forceinline__ void load_piece(uint4 (&buf)[kScatterVecs], const uint4* xrow, int v0,
+                                           int nvec) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < kScatterVecs; ++j) {
+    const int v = v0 + j * 32 + lane;
+    if (v < nvec) buf[j] = ld_once(xrow + v);
+  }
+}
+
+template <bool kPre>
 __device__ __forceinline__ void copy_token(const DispatchParams& p, const SourceDesc& src, int t,
-                                           int code) {
+                                           int code, const uint4 (&pre)[kScatterVecs]) {
   const int lane = threadIdx.x & 31;
   const int K = p.K;
   const int nvec = p.row_bytes >> 4;
   const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
   for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
     uint4 buf[kScatterVecs];
+    if (kPre && v0 == 0) {
 #pragma unroll
-    for (int j = 0; j < kScatterVecs; ++j) {
-      const int v = v0 + j * 32 + lane;
-      if (v < nvec) buf[j] = ld_once(xrow + v);
+      for (int j = 0; j < kScatterVecs; ++j) buf[j] = pre[j];
+    } else {
+      load_piece(buf, xrow, v0, nvec);
     }
     for (int k = 0; k < K; ++k) {
       const int c = __shfl_sync(0xffffffffu, code, k);
@@ -180,6 +194,44 @@ __device__ __forceinline__ int write_route(const DispatchParams& p, int s, int t
   const int code = (f << kWorkerShift) | row;
   p.routes[(int64_t)gt * p.K + lane] = make_int2(code, __float_as_int(w));
   return code;
+}
+
+// One token of the scatter: finish each route's row from the layout (the
+// chunk's first row of the expert plus the route's rank inside the chunk),
+// write the receipt, copy the row. kPre: the row's first piece and the
+// weights were loaded early into pre / pre_w.
+template <bool kPre, typename RowOf>
+__device__ __forceinline__ void scatter_token(const DispatchParams& p, int gt, RowOf row_of,
+                                              float pre_w, const uint4 (&pre)[kScatterVecs]) {
+  const int lane = threadIdx.x & 31;
+  const int K = p.K;
+  const int s = source_of_token(p, gt);
+  const SourceDesc& src = p.src[s];
+  const int t = gt - src.tok_off;
+  int code = -1;
+  if (lane < K) {
+    int e = -1, row = 0;
+    if (row_of(gt, s, t, e, row)) {
+      const float w = kPre ? pre_w : src.w[(int64_t)t * K + lane];
+      code = write_route(p, s, t, gt, e, row, w);
+    } else {
+      p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+    }
+  }
+  copy_token<kPre>(p, src, t, code, pre);
+}
+
+// Loads warp `gwarp`'s first token's first row piece and weights.
+__device__ __forceinline__ bool preload_first(const DispatchParams& p, int gwarp,
+                                              uint4 (&pre)[kScatterVecs], float& pre_w) {
+  if (gwarp >= p.total_tokens) return false;
+  const int lane = threadIdx.x & 31;
+  const int s0 = source_of_token(p, gwarp);
+  const int t0 = gwarp - p.src[s0].tok_off;
+  load_piece(pre, reinterpret_cast<const uint4*>(p.src[s0].x + (int64_t)t0 * p.row_bytes), 0,
+             p.row_bytes >> 4);
+  if (lane < p.K) pre_w = p.src[s0].w[(int64_t)t0 * p.K + lane];
+  return true;
 }
 
 // ---------------------------------------------------------------- large path
@@ -307,14 +359,20 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
   if (threadIdx.x == 0) *p.done = 0u;
 }
 
-__global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ DispatchParams p) {
+__global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(16) int32_t ssm[];
   pdl_launch_dependents();
-  pdl_wait();  // the layout kernel's outputs
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int K = p.K, E = p.E, G = p.total_chunks;
+
+  // The source rows and weights are inputs, not layout outputs: start loading
+  // this warp's first token while the layout kernel is still running.
+  uint4 pre[kScatterVecs];
+  float pre_w = 0.0f;
+  const bool have_pre = preload_first(p, gwarp, pre, pre_w);
+  pdl_wait();  // the layout kernel's outputs
 
   // With few chunk counts, each block turns them into chunk starting rows in
   // shared memory (one parallel read from L2) instead of waiting for a
@@ -346,25 +404,20 @@ __global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ Di
     ends = sh_total;
   }
 
-  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
-    const int s = source_of_token(p, gt);
-    const SourceDesc& src = p.src[s];
-    const int t = gt - src.tok_off;
-    int code = -1;
-    if (lane < K) {
-      const int rt = p.route_tmp[(int64_t)gt * K + lane];
-      if (rt >= 0) {
-        const int e = rt >> kRankBits;
-        const int rank = rt & ((1 << kRankBits) - 1);
-        const int g = src.chunk_off + t / kChunk;
-        const int row = chunk_start[g * E + e] + rank;
-        code = write_route(p, s, t, gt, e, row, src.w[(int64_t)t * K + lane]);
-      } else {
-        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
-      }
-    }
-    copy_token(p, src, t, code);
+  auto row_of = [&](int gt, int s, int t, int& e, int& row) -> bool {
+    const int rt = p.route_tmp[(int64_t)gt * K + lane];
+    if (rt < 0) return false;
+    e = rt >> kRankBits;
+    const int g = p.src[s].chunk_off + t / kChunk;
+    row = chunk_start[g * E + e] + (rt & ((1 << kRankBits) - 1));
+    return true;
+  };
+  int gt = gwarp;
+  if (have_pre) {
+    scatter_token<true>(p, gt, row_of, pre_w, pre);
+    gt += nwarps;
   }
+  for (; gt < p.total_tokens; gt += nwarps) scatter_token<false>(p, gt, row_of, 0.0f, pre);
   fill_padding(p, ends);
 }
 
@@ -384,6 +437,14 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long* err = blockIdx.x == 0 ? p.err : nullptr;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+
+  // Load this warp's first row and weights now, so that their latency
+  // overlaps the counting below.
+  uint4 pre[kScatterVecs];
+  float pre_w = 0.0f;
+  const bool have_pre = preload_first(p, gwarp, pre, pre_w);
 
   // Pass 1 (every block, all routes): ranks inside each chunk, chunk counts.
   for (int c = 0; c < G; ++c) {
@@ -441,25 +502,19 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   __syncthreads();
 
   // Pass 2: this block's share of the tokens.
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int gt = gwarp; gt < N; gt += nwarps) {
-    const int s = source_of_token(p, gt);
-    const SourceDesc& src = p.src[s];
-    const int t = gt - src.tok_off;
-    int code = -1;
-    if (lane < K) {
-      const uint32_t info = rinfo[gt * K + lane];
-      if (info != ~0u) {
-        const int e = (int)(info >> kRankBits);
-        const int row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
-        code = write_route(p, s, t, gt, e, row, src.w[(int64_t)t * K + lane]);
-      } else {
-        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
-      }
-    }
-    copy_token(p, src, t, code);
+  auto row_of = [&](int gt, int, int, int& e, int& row) -> bool {
+    const uint32_t info = rinfo[gt * K + lane];
+    if (info == ~0u) return false;
+    e = (int)(info >> kRankBits);
+    row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
+    return true;
+  };
+  int gt = gwarp;
+  if (have_pre) {
+    scatter_token<true>(p, gt, row_of, pre_w, pre);
+    gt += nwarps;
   }
+  for (; gt < N; gt += nwarps) scatter_token<false>(p, gt, row_of, 0.0f, pre);
 
   // Padding rows, from this block's own copy of the layout.
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
@@ -512,7 +567,7 @@ cudaError_t configure_dispatch_kernels() {
                              kSmallSmemMax);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)scatter_smem(kBlockScanMax, kMaxExperts));
+                             (int)scatter_smem(AFD_BLOCK_SCAN_MAX, kMaxExperts));
   return e;
 }
 
@@ -529,16 +584,17 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
                   false, p);
   }
   DispatchParams q = p;
-  q.block_scan = (int64_t)p.total_chunks * p.E <= kBlockScanMax ? 1 : 0;
+  q.block_scan = (int64_t)p.total_chunks * p.E <= AFD_BLOCK_SCAN_MAX ? 1 : 0;
   const int lgrid = q.total_chunks > 0 ? q.total_chunks : 1;
   cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(q.E), stream, false, q);
   if (e != cudaSuccess) return e;
-  // four warps (tokens) per block, so that blocks spread evenly over the SMs
-  int grid = (q.total_tokens + 3) / 4;
-  if (grid > sm_cap * 8) grid = sm_cap * 8;
+  // small blocks, a warp per token, so that blocks spread evenly over the SMs
+  constexpr int kWarps = AFD_SCATTER_BLOCK / 32;
+  int grid = (q.total_tokens + kWarps - 1) / kWarps;
+  if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
   const size_t smem = q.block_scan ? scatter_smem(q.total_chunks * q.E, q.E) : 0;
-  return launch(scatter_kernel, grid, 128, smem, stream, true, q);
+  return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, smem, stream, true, q);
 }
 
 }  // namespace afd

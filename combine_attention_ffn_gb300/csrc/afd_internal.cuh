@@ -18,7 +18,17 @@ constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
 constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
 constexpr int kSmallRoutes = 4096;   // exchanges up to this many routes take the one-kernel dispatch
 constexpr int kSmallSmemMax = 110 * 1024;
-constexpr int kBlockScanMax = 8192;  // chunk x expert counts each scatter block scans itself
+// Launch-shape constants. They only change speed, never results; a build may
+// override them (-D...) to compare shapes.
+#ifndef AFD_BLOCK_SCAN_MAX
+#define AFD_BLOCK_SCAN_MAX 8192  // chunk x expert counts each scatter block scans itself
+#endif
+#ifndef AFD_SCATTER_BLOCK
+#define AFD_SCATTER_BLOCK 128    // threads per scatter block (a warp per token)
+#endif
+#ifndef AFD_TOKEN_COMBINE_MIN
+#define AFD_TOKEN_COMBINE_MIN 8  // x SMs: tokens from which the per-token combine is used
+#endif
 static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 
 constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
