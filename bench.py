@@ -20,7 +20,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -146,6 +145,18 @@ class ClockSampler:
                 "window": "1 s of back-to-back replays just before the timed region, and the region"}
 
 
+def reduce_max(value: float, device) -> float:
+    """The slowest rank's value (replicas: every rank timed its own exchange)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -194,7 +205,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl),
+        "config": workload_config(wl, execution="CPU oracle (single-threaded C) on the host",
+                                  l2="not applicable"),
         "gbs": round(ab["total"] / (value * 1e-6) / 1e9, 2),
         "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle"},
@@ -204,15 +216,15 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl) -> dict:
+def workload_config(wl, execution: str = "one CUDA graph per round trip",
+                    l2: str = "flushed before every timed step (256 MB write, outside the step's events)") -> dict:
     return {"workload": f"{wl.name}: A={wl.A} sources x T={wl.T[0]} tokens, F={wl.F} workers, "
                         f"E={wl.E}, K={wl.K}, H={wl.H}, {wl.dtype}, alpha={wl.alpha}, "
                         f"bucket={wl.bucket}, {wl.routing} routing",
             "A": wl.A, "F": wl.F, "E": wl.E, "K": wl.K, "H": wl.H, "T_per_source": wl.T[0],
             "bucket": wl.bucket, "expert_alignment": wl.alpha, "routing": wl.routing,
             "expert": "identity (reply = received rows)",
-            "l2": "flushed before every timed step (256 MB write, outside the step's events)",
-            "execution": "one CUDA graph per round trip"}
+            "l2": l2, "execution": execution}
 
 
 # ------------------------------------------------------------------ our arm
@@ -251,39 +263,46 @@ def main():
     ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s, T in enumerate(wl.T)]
     outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for T in wl.T]
 
-    def exchange(phase_events=None):
-        if phase_events:
-            phase_events[0].record()
+    def dispatch_all():
         for s in range(wl.A):
             buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
-        if phase_events:
-            phase_events[1].record()
+
+    def receive_reply_all():
         for f in range(wl.F):
             r = buf.worker_receive(f, bucket=wl.bucket)
-            buf.worker_reply(f, r.rows, r.receipt)
-        if phase_events:
-            phase_events[2].record()
+            buf.worker_reply(f, r.rows, r.receipt)  # identity expert
+
+    def collect_all():
         for s in range(wl.A):
             buf.source_collect(s, out=outs[s])
-        if phase_events:
-            phase_events[3].record()
 
-    # warm up eagerly, then capture one round trip (with phase events inside
-    # the graph when this PyTorch can record them as graph nodes)
+    def exchange():
+        dispatch_all()
+        receive_reply_all()
+        collect_all()
+
+    # warm up eagerly, then capture one round trip as one graph (the headline),
+    # and one more exchange as three graphs, one per phase, for the per-kernel
+    # times (an event between kernels inside one graph would cut the
+    # programmatic-launch edges and slow the headline down)
     for _ in range(2):
         exchange()
     torch.cuda.synchronize()
-    try:
-        phase = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-    except TypeError:
-        phase = None
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        exchange(phase)
+        exchange()
+    g_phase = []
+    for fn in (dispatch_all, receive_reply_all, collect_all):
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp):
+            fn()
+        g_phase.append(gp)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         g.replay()
+        for gp in g_phase:
+            gp.replay()
     torch.cuda.synchronize()
     # The timed region is short next to nvidia-smi's sampling period, so the
     # sampler also covers one second of back-to-back replays just before it.
@@ -295,62 +314,67 @@ def main():
             g.replay()
         torch.cuda.synchronize()
 
-    # timed region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    phase_ms = {"dispatch": [], "combine": []}
+    # timed region: each step is one replay of the round trip, L2 flushed
+    # before it; after it (outside the step's events) the same exchange runs
+    # phase by phase for the per-kernel times
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    steps_ev = [(ev(), ev()) for _ in range(args.steps)]
+    phase_ev = [[ev() for _ in range(4)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
-        ev[i][0].record()
+        steps_ev[i][0].record()
         g.replay()
-        ev[i][1].record()
-        if phase is not None:
-            torch.cuda.synchronize()
-            phase_ms["dispatch"].append(phase[0].elapsed_time(phase[1]))
-            phase_ms["combine"].append(phase[2].elapsed_time(phase[3]))
+        steps_ev[i][1].record()
+        flush.zero_()
+        pe = phase_ev[i]
+        pe[0].record()
+        for j, gp in enumerate(g_phase):
+            gp.replay()
+            pe[j + 1].record()
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    step_ms = [a.elapsed_time(b) for a, b in steps_ev]
+    ms = reduce_max(sum(step_ms) / len(step_ms), dev)
+    d_ms = statistics.mean(pe[0].elapsed_time(pe[1]) for pe in phase_ev)
+    r_ms = statistics.mean(pe[1].elapsed_time(pe[2]) for pe in phase_ev)
+    c_ms = statistics.mean(pe[2].elapsed_time(pe[3]) for pe in phase_ev)
 
     ab = algorithmic_bytes(wl, inp)
     peak, peak_kind = load_peaks()
     us = ms * 1e3
     launches_per_step = (1 if buf_small else 2) + (wl.A if wl.F > 1 else 1 + wl.A)
 
-    # dominant kernel: the phase with the larger share; per-launch bytes and time
-    roofline = None
-    if phase is not None and phase_ms["combine"]:
-        d_ms = statistics.mean(phase_ms["dispatch"])
-        c_ms = statistics.mean(phase_ms["combine"])
-        if c_ms >= d_ms:
-            n_launch = wl.A if wl.F > 1 else 1
-            per_launch_s = c_ms / n_launch * 1e-3
-            per_launch_bytes = ab["combine"] / n_launch
-            kname = "combine"
-        else:
-            per_launch_s = d_ms * 1e-3
-            per_launch_bytes = ab["dispatch"]
-            kname = "dispatch (layout + scatter)"
-        achieved = per_launch_bytes / per_launch_s / 1e9
-        traffic = kernel_traffic("combine" if kname == "combine" else "scatter", f"{wl.name}-T{wl.T[0]}")
-        roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
-                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": traffic,
-                    "bytes_per_launch": int(per_launch_bytes),
-                    "us_per_launch": round(per_launch_s * 1e6, 2),
-                    "phase_us": {"dispatch": round(d_ms * 1e3, 2), "combine": round(c_ms * 1e3, 2)}}
+    # dominant kernel: the phase with the larger share of the time
+    comb_ms = r_ms + c_ms  # F = 1 combines at reply, F > 1 at collect
+    if comb_ms >= d_ms:
+        n_launch = wl.A if wl.F > 1 else 1
+        per_launch_s = comb_ms / n_launch * 1e-3
+        per_launch_bytes = ab["combine"] / n_launch
+        kname = "combine"
+    else:
+        per_launch_s = d_ms * 1e-3
+        per_launch_bytes = ab["dispatch"]
+        kname = "dispatch (layout + scatter)" if not buf_small else "dispatch (one kernel)"
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    traffic = kernel_traffic("combine" if kname == "combine" else "scatter", f"{wl.name}-T{wl.T[0]}")
+    roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "bytes_per_launch": int(per_launch_bytes),
+                "us_per_launch": round(per_launch_s * 1e6, 2),
+                "phase_us": {"dispatch": round(d_ms * 1e3, 2),
+                             "receive_reply": round(r_ms * 1e3, 2),
+                             "collect": round(c_ms * 1e3, 2)},
+                "note": "per-phase graphs replayed after each timed step, L2 flushed first"}
 
     # end to end through the public API, host buffers, copies inside the region
     e2e = None
@@ -381,7 +405,8 @@ def main():
             "peak_gbs": peak, "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": 2 * launches_per_step * args.steps,
+            "gpu_launches_note": "per step: the round-trip graph plus the same exchange phase by phase",
             "wall_s": round(wall, 3),
             "context": ({"pages_4xH100_nvlink_us": ctx,
                          "note": "multi-GPU communication-only figure from the pages; not this workload"}

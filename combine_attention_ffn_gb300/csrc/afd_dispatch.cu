@@ -20,12 +20,11 @@
 //  * small exchanges (at most kSmallRoutes routes): one kernel. Every block
 //    counts all routes itself (they are few and sit in L2), scans in shared
 //    memory, then copies its share of the rows. No block waits for another.
-//  * large exchanges: layout_kernel (one block per chunk of 256 tokens) then
-//    scatter_kernel (a warp per token), launched as a programmatic dependent
-//    so that its launch overlaps the layout. When the chunk x expert counts
-//    are few (at most kBlockScanMax), every scatter block reads them and
-//    scans them in shared memory; otherwise the last layout block to finish
-//    (found with a completion counter; nobody waits) scans them once.
+//  * large exchanges: layout_kernel (one block per chunk of 256 tokens; the
+//    last block to finish, found with a completion counter, scans the chunk
+//    counts; nobody waits) then scatter_kernel (a warp per token), launched
+//    as a programmatic dependent: its blocks start early and load their first
+//    source rows while the layout is still running.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -346,8 +345,6 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
     }
   }
 
-  if (p.block_scan) return;  // every scatter block scans the chunk counts itself
-
   // The last block to arrive finishes the layout; nobody waits.
   __threadfence();
   __syncthreads();
@@ -360,12 +357,11 @@ __global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ 
 }
 
 __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid_constant__ DispatchParams p) {
-  extern __shared__ __align__(16) int32_t ssm[];
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, E = p.E, G = p.total_chunks;
+  const int K = p.K, E = p.E;
 
   // The source rows and weights are inputs, not layout outputs: start loading
   // this warp's first token while the layout kernel is still running.
@@ -373,36 +369,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   float pre_w = 0.0f;
   const bool have_pre = preload_first(p, gwarp, pre, pre_w);
   pdl_wait();  // the layout kernel's outputs
-
-  // With few chunk counts, each block turns them into chunk starting rows in
-  // shared memory (one parallel read from L2) instead of waiting for a
-  // separate scan: cstart[g][e], totals, then the aligned starts.
-  int32_t* cstart = ssm;              // [G][E]
-  int32_t* sh_total = cstart + G * E; // [E]
-  int32_t* sh_start = sh_total + E;   // [E]
   const int32_t* chunk_start = p.chunk_start;
-  const int32_t* ends = p.ends;
-  if (p.block_scan) {
-    for (int i = threadIdx.x; i < G * E; i += blockDim.x) cstart[i] = __ldcg(p.chunk_counts + i);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int run = 0;
-      for (int g = 0; g < G; ++g) {
-        const int v = cstart[g * E + e];
-        cstart[g * E + e] = run;
-        run += v;
-      }
-      sh_total[e] = run;
-    }
-    __syncthreads();
-    worker_scan(p, sh_total, sh_start, blockIdx.x == 0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * E; i += blockDim.x) cstart[i] += sh_start[i % E];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
-    __syncthreads();
-    chunk_start = cstart;
-    ends = sh_total;
-  }
 
   auto row_of = [&](int gt, int s, int t, int& e, int& row) -> bool {
     const int rt = p.route_tmp[(int64_t)gt * K + lane];
@@ -418,7 +385,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
     gt += nwarps;
   }
   for (; gt < p.total_tokens; gt += nwarps) scatter_token<false>(p, gt, row_of, 0.0f, pre);
-  fill_padding(p, ends);
+  fill_padding(p, p.ends);
 }
 
 // ---------------------------------------------------------------- small path
@@ -528,8 +495,6 @@ size_t layout_smem(int E) {
   return count > finish ? count : finish;
 }
 
-size_t scatter_smem(int GE, int E) { return (size_t)(GE + 2 * E) * sizeof(int32_t); }
-
 size_t small_smem(int E, int N, int K) {
   const int G = (N + kChunk - 1) / kChunk;
   return (size_t)kChunkWarps * E * 4 + (size_t)N * K * 4 + (size_t)2 * E * 4 +
@@ -565,9 +530,6 @@ cudaError_t configure_dispatch_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)scatter_smem(AFD_BLOCK_SCAN_MAX, kMaxExperts));
   return e;
 }
 
@@ -583,18 +545,15 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
     return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,
                   false, p);
   }
-  DispatchParams q = p;
-  q.block_scan = (int64_t)p.total_chunks * p.E <= AFD_BLOCK_SCAN_MAX ? 1 : 0;
-  const int lgrid = q.total_chunks > 0 ? q.total_chunks : 1;
-  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(q.E), stream, false, q);
+  const int lgrid = p.total_chunks > 0 ? p.total_chunks : 1;
+  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(p.E), stream, false, p);
   if (e != cudaSuccess) return e;
   // small blocks, a warp per token, so that blocks spread evenly over the SMs
   constexpr int kWarps = AFD_SCATTER_BLOCK / 32;
-  int grid = (q.total_tokens + kWarps - 1) / kWarps;
+  int grid = (p.total_tokens + kWarps - 1) / kWarps;
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
-  const size_t smem = q.block_scan ? scatter_smem(q.total_chunks * q.E, q.E) : 0;
-  return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, smem, stream, true, q);
+  return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
 }
 
 }  // namespace afd

@@ -20,9 +20,6 @@ constexpr int kSmallRoutes = 4096;   // exchanges up to this many routes take th
 constexpr int kSmallSmemMax = 110 * 1024;
 // Launch-shape constants. They only change speed, never results; a build may
 // override them (-D...) to compare shapes.
-#ifndef AFD_BLOCK_SCAN_MAX
-#define AFD_BLOCK_SCAN_MAX 8192  // chunk x expert counts each scatter block scans itself
-#endif
 #ifndef AFD_SCATTER_BLOCK
 #define AFD_SCATTER_BLOCK 128    // threads per scatter block (a warp per token)
 #endif
@@ -63,7 +60,6 @@ struct DispatchParams {
   int32_t total_tokens;  // sum of T
   int32_t total_chunks;  // sum of ceil(T / kChunk)
   int64_t R_arena;       // rows per worker arena
-  int32_t block_scan;    // 1: every scatter block scans the chunk counts itself
   // context scratch
   int32_t* route_tmp;    // [total_tokens][K]: (expert << 8 | rank in chunk) or -1
   int32_t* chunk_counts; // [total_chunks][E]
