@@ -30,7 +30,7 @@ BF16, FP8_E4M3 = 0, 1
 EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_worker_receive",
            "afd_worker_reply", "afd_source_collect", "afd_get_error", "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
-           "afd_recv_rows_for_bucket", "afd_version")
+           "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc")
 
 
 class AfdError(RuntimeError):
@@ -87,6 +87,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_arena_rows": (i64, [v]),
         "afd_recv_rows_for_bucket": (i64, [v, i32]),
         "afd_version": (i32, []),
+        "afd_route_layout_noalloc": (i32, [v, i32, i32, i32, i32, i32, v, v, v, v]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -289,3 +290,22 @@ class Buffer:
         completes) once no tensor viewing it is alive."""
         self._ctx = None
         self._h = ctypes.c_void_p()
+
+
+def route_layout_noalloc(ids: torch.Tensor, num_experts: int, num_workers: int,
+                         expert_alignment: int, ends: torch.Tensor, slots: torch.Tensor,
+                         error: torch.Tensor, stream=None) -> None:
+    """Routing layout into caller-provided outputs; the library allocates
+    nothing (its scratch is a fixed device array). See
+    afd_route_layout_noalloc in include/afd.h for the limits and rules."""
+    lib = load_library()
+    T, K = (int(ids.shape[0]), int(ids.shape[1])) if ids.dim() == 2 else (0, 1)
+    for name, t, dt in (("ends", ends, torch.int32), ("slots", slots, torch.int32),
+                        ("error", error, torch.int32), ("ids", ids, torch.int64)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise AfdError(ERR_ARG, f"{name} must be contiguous {dt}")
+    st = lib.afd_route_layout_noalloc(_ptr(ids) if T else None, T, K, num_experts, num_workers,
+                                      expert_alignment, _ptr(ends), _ptr(slots) if T else None,
+                                      _ptr(error), _stream_handle(stream, ids.device))
+    if st != OK:
+        raise AfdError(st, "afd_route_layout_noalloc: " + lib.afd_status_string(st).decode())

@@ -241,6 +241,37 @@ AFD_API int64_t afd_arena_rows(const afd_ctx* ctx);
 /* Receive shape for `bucket` with read_host_counts = 0. */
 AFD_API int64_t afd_recv_rows_for_bucket(const afd_ctx* ctx, int32_t bucket);
 
+/* Routing layout without allocation (no counterpart in the pages). Some
+ * callers cannot call cudaMalloc: code that runs inside another framework's
+ * memory pool or allocator hook, or a process whose device memory is fully
+ * reserved up front. This call allocates nothing, through the CUDA runtime or
+ * any library: its scratch (about 1.5 MiB) is a fixed device array inside
+ * libafd, which every GPU that loads the library holds until the process
+ * exits. It computes, for one source's routing, what the dispatch layout
+ * computes: route checks, per-worker ends[] with expert_alignment padding,
+ * and the row of every valid route (expert-major; inside an expert, token
+ * order), without moving any payload.
+ *   ids        device int64 [num_tokens, top_k]; IDs in [0, num_experts) or -1
+ *   ends       device int32 [num_experts] out: per worker f, ends[f*E/F + l]
+ *              is local expert l's end (same convention as afd_recv.ends)
+ *   slots      device int32 [num_tokens, top_k] out: the route's row inside
+ *              its worker (worker = ID / (E/F)), or -1 (skipped or invalid)
+ *   error      device int32 [3] out: {code, token, k} of the first invalid
+ *              route in (token, k) order (code AFD_ERR_ROUTE_RANGE or
+ *              AFD_ERR_ROUTE_DUP), or {AFD_OK, -1, -1}
+ * Limits: num_tokens <= 8192, top_k <= 32, num_tokens * top_k <= 65536,
+ * num_experts <= 1024; larger sizes return AFD_ERR_UNSUPPORTED and enqueue
+ * nothing. Work is enqueued on `stream` (the current device's).
+ * The first call on a device looks up the scratch array's device address
+ * (and sets a kernel attribute); make that first call before any stream
+ * capture on that device. All calls on a device share the one scratch array:
+ * calls whose GPU work overlaps (different streams without ordering) race and
+ * give wrong results; order them. */
+AFD_API afd_status afd_route_layout_noalloc(const int64_t* ids, int32_t num_tokens, int32_t top_k,
+                                            int32_t num_experts, int32_t num_workers,
+                                            int32_t expert_alignment, int32_t* ends,
+                                            int32_t* slots, int32_t* error, afd_stream stream);
+
 /* Library version, (major << 16) | minor. */
 AFD_API int32_t afd_version(void);
 
