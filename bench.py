@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--profile-exchanges", type=int, default=0,
+                    help="run this many eager exchanges of the workload and exit "
+                         "(a short, untimed program for an external profiler)")
     return ap.parse_args()
 
 
@@ -281,6 +284,14 @@ def main():
         receive_reply_all()
         collect_all()
 
+    if args.profile_exchanges:
+        for _ in range(args.profile_exchanges):
+            exchange()
+        torch.cuda.synchronize()
+        buf.close()
+        print(f"ran {args.profile_exchanges} exchanges of {wl.name} T={wl.T[0]}")
+        return 0
+
     # warm up eagerly, then capture one round trip as one graph (the headline),
     # and one more exchange as three graphs, one per phase, for the per-kernel
     # times (an event between kernels inside one graph would cut the
@@ -353,19 +364,17 @@ def main():
     us = ms * 1e3
     launches_per_step = (1 if buf_small else 2) + (wl.A if wl.F > 1 else 1 + wl.A)
 
-    # dominant kernel: the phase with the larger share of the time
+    # dominant kernel: the combine has the largest share of the launch list
+    # (profiles/launches_*.md); one launch per source for F > 1, one for all
+    # sources for F = 1. The dispatch phase (layout + scatter) is reported too.
     comb_ms = r_ms + c_ms  # F = 1 combines at reply, F > 1 at collect
-    if comb_ms >= d_ms:
-        n_launch = wl.A if wl.F > 1 else 1
-        per_launch_s = comb_ms / n_launch * 1e-3
-        per_launch_bytes = ab["combine"] / n_launch
-        kname = "combine"
-    else:
-        per_launch_s = d_ms * 1e-3
-        per_launch_bytes = ab["dispatch"]
-        kname = "dispatch (layout + scatter)" if not buf_small else "dispatch (one kernel)"
+    n_launch = wl.A if wl.F > 1 else 1
+    per_launch_s = comb_ms / n_launch * 1e-3
+    per_launch_bytes = ab["combine"] / n_launch
+    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 8 * 152 else "combine_kernel"
     achieved = per_launch_bytes / per_launch_s / 1e9
-    traffic = kernel_traffic("combine" if kname == "combine" else "scatter", f"{wl.name}-T{wl.T[0]}")
+    traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}")
+    d_gbs = ab["dispatch"] / (d_ms * 1e-3) / 1e9
     roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -374,6 +383,8 @@ def main():
                 "phase_us": {"dispatch": round(d_ms * 1e3, 2),
                              "receive_reply": round(r_ms * 1e3, 2),
                              "collect": round(c_ms * 1e3, 2)},
+                "dispatch_phase": {"us": round(d_ms * 1e3, 2), "bytes": int(ab["dispatch"]),
+                                   "achieved": round(d_gbs, 1), "frac": round(d_gbs / peak, 4)},
                 "note": "per-phase graphs replayed after each timed step, L2 flushed first"}
 
     # end to end through the public API, host buffers, copies inside the region
