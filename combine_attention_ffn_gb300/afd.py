@@ -27,7 +27,8 @@ OK, ERR_ARG, ERR_STATE, ERR_BUCKET, ERR_RECEIPT = 0, 1, 2, 3, 4
 ERR_ROUTE_RANGE, ERR_ROUTE_DUP, ERR_CUDA, ERR_OOM, ERR_CAPTURING, ERR_UNSUPPORTED = 5, 6, 7, 8, 9, 10
 BF16, FP8_E4M3 = 0, 1
 
-EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_worker_receive",
+EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispatch_cached",
+           "afd_worker_receive",
            "afd_worker_reply", "afd_source_collect", "afd_get_error", "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
            "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc")
@@ -76,6 +77,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_create": (i32, [P(Config), i32, P(v)]),
         "afd_destroy": (i32, [v]),
         "afd_source_dispatch": (i32, [v, i32, v, v, v, v, i64, i64, i32, i32, i32, v]),
+        "afd_source_dispatch_cached": (i32, [v, i32, v, v, v, i64, i64, i32, i32, i32, v]),
         "afd_worker_receive": (i32, [v, i32, i32, i32, v, P(Recv)]),
         "afd_worker_reply": (i32, [v, i32, v, i64, u64, v]),
         "afd_source_collect": (i32, [v, i32, v, i32, v, P(View)]),
@@ -222,6 +224,32 @@ class Buffer:
                                            int(bool(read_host_counts)),
                                            _stream_handle(stream, self.device))
         self._check(st, "source_dispatch")
+
+    def source_dispatch_cached(self, source: int, x: torch.Tensor, weights: Optional[torch.Tensor] = None,
+                               x_scale: Optional[torch.Tensor] = None, *, bucket: int,
+                               read_host_counts: bool = False, stream=None) -> None:
+        """Dispatch with the routing (IDs, layout, receipts) of the last exchange;
+        only the rows move. `weights` replaces the routing weights of the same
+        IDs, or None keeps them."""
+        T = int(x.shape[0]) if x is not None else 0
+        if T:
+            want = torch.float8_e4m3fn if self.dtype == "fp8" else torch.bfloat16
+            if x.dtype != want or tuple(x.shape) != (T, self.H) or not x.is_contiguous():
+                raise AfdError(ERR_ARG, f"x must be contiguous {want} [T, {self.H}]")
+            if weights is not None and (weights.dtype != torch.float32 or
+                                        tuple(weights.shape) != (T, self.K) or not weights.is_contiguous()):
+                raise AfdError(ERR_ARG, f"weights must be contiguous float32 [T, {self.K}]")
+        sst = ssb = 0
+        if x_scale is not None:
+            if x_scale.dtype != torch.float32 or tuple(x_scale.shape) != (T, self.H // 128):
+                raise AfdError(ERR_ARG, f"x_scale must be float32 [T, {self.H // 128}]")
+            sst, ssb = x_scale.stride()
+        st = self._lib.afd_source_dispatch_cached(self._h, source, _ptr(x) if T else None,
+                                                  _ptr(weights) if T else None,
+                                                  _ptr(x_scale) if T else None, sst, ssb, T, bucket,
+                                                  int(bool(read_host_counts)),
+                                                  _stream_handle(stream, self.device))
+        self._check(st, "source_dispatch_cached")
 
     def worker_receive(self, worker: int, *, bucket: int, read_host_counts: bool = False,
                        stream=None) -> Receive:

@@ -489,6 +489,36 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   fill_padding(p, sh_total);
 }
 
+// ---------------------------------------------------------------- cached path
+
+// Dispatch with the previous exchange's routing: the receipt already holds
+// every route's row, so a warp per token only copies the row (and, when new
+// weights are given, refreshes the weights in both receipts).
+__global__ void __launch_bounds__(AFD_SCATTER_BLOCK) cached_scatter_kernel(const __grid_constant__ DispatchParams p) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;
+  uint4 none[kScatterVecs];
+  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
+    const int s = source_of_token(p, gt);
+    const SourceDesc& src = p.src[s];
+    const int t = gt - src.tok_off;
+    int code = -1;
+    if (lane < K) {
+      int2* r = p.routes + (int64_t)gt * K + lane;
+      code = r->x;
+      if (src.w != nullptr && code >= 0) {
+        const float w = src.w[(int64_t)t * K + lane];
+        r->y = __float_as_int(w);
+        p.row_w[(int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)] = w;
+      }
+    }
+    copy_token<false>(p, src, t, code, none);
+  }
+}
+
 size_t layout_smem(int E) {
   const size_t count = (size_t)kChunkWarps * E * (sizeof(uint32_t) + sizeof(uint16_t));
   const size_t finish = (size_t)(kChunk + 2 * E) * sizeof(int32_t);
@@ -554,6 +584,20 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
   return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
+}
+
+}  // namespace afd
+
+namespace afd {
+
+// Launched normally (not as a programmatic dependent): it rewrites the rows
+// that the previous exchange's combine reads.
+cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
+  constexpr int kWarps = AFD_SCATTER_BLOCK / 32;
+  int grid = (p.total_tokens + kWarps - 1) / kWarps;
+  if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
+  if (grid < 1) grid = 1;
+  return launch(cached_scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, false, p);
 }
 
 }  // namespace afd

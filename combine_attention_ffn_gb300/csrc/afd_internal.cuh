@@ -96,6 +96,7 @@ struct CopyParams {
 // Launchers (return the launch's cudaError_t).
 bool dispatch_is_small(const DispatchParams& p);
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream);
+cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t configure_dispatch_kernels();

@@ -73,6 +73,11 @@ struct afd_ctx {
   int phase;
   int bucket;
   int rhc;
+  bool cached;          // this exchange reuses the last layout
+  // the last layout that a dispatch computed (what a cached dispatch reuses)
+  bool layout_valid;
+  int layout_bucket;
+  int32_t layout_T[afd::kMaxSources];
   int staged_n;
   int replied_n;
   int collected_n;
@@ -157,6 +162,7 @@ int64_t recv_rows_for(const afd_ctx* c, int64_t bucket) {
 
 void reset_exchange(afd_ctx* c) {
   c->phase = kIdle;
+  c->cached = false;
   c->staged_n = c->replied_n = c->collected_n = 0;
   c->bucket = -1;
   c->rhc = -1;
@@ -212,6 +218,60 @@ afd_status check_config(const afd_config* g, afd_ctx* c) {
   if (g->dtype != AFD_BF16 && g->dtype != AFD_FP8_E4M3)
     return fail(c, AFD_ERR_ARG, "dtype must be AFD_BF16 or AFD_FP8_E4M3");
   if (g->num_sms < 0) return fail(c, AFD_ERR_ARG, "num_sms must be >= 0");
+  return AFD_OK;
+}
+
+// Builds the exchange's launch parameters from the staged sources and
+// launches its dispatch: the layout and scatter, or (cached) only the copy of
+// the rows along the last layout.
+afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached) {
+  const afd_config& g = c->cfg;
+  DispatchParams p;
+  memset(&p, 0, sizeof p);
+  int tok = 0, chunks = 0;
+  for (int s = 0; s < g.num_sources; ++s) {
+    p.src[s] = c->src[s];
+    p.src[s].tok_off = tok;
+    p.src[s].chunk_off = chunks;
+    c->src[s].tok_off = tok;
+    c->src[s].chunk_off = chunks;
+    tok += c->src[s].T;
+    chunks += (c->src[s].T + afd::kChunk - 1) / afd::kChunk;
+  }
+  p.A = g.num_sources;
+  p.F = g.num_workers;
+  p.E = g.num_experts;
+  p.Ef = c->Ef;
+  p.K = g.top_k;
+  p.alpha = g.expert_alignment;
+  p.bucket = c->bucket;
+  p.row_bytes = c->row_bytes;
+  p.nscale = c->nscale;
+  p.total_tokens = tok;
+  p.total_chunks = chunks;
+  p.R_arena = c->R_arena;
+  p.route_tmp = c->route_tmp;
+  p.chunk_counts = c->chunk_counts;
+  p.chunk_start = c->chunk_start;
+  p.done = c->done;
+  p.err = c->err;
+  p.starts = c->starts;
+  p.ends = c->ends;
+  p.hcounts = c->hcounts;
+  p.routes = c->routes;
+  p.row_src = c->row_src;
+  p.row_w = c->row_w;
+  p.rows = c->rows;
+  p.row_scales = c->row_scales;
+  cudaError_t e = cached ? afd::launch_cached_scatter(p, c->sm_cap, stream)
+                         : afd::launch_dispatch(p, c->sm_cap, stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "dispatch launch");
+  if (!cached) {
+    c->layout_valid = true;
+    c->layout_bucket = c->bucket;
+    for (int s = 0; s < g.num_sources; ++s) c->layout_T[s] = c->src[s].T;
+  }
+  c->phase = kDispatched;
   return AFD_OK;
 }
 
@@ -358,6 +418,8 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
   if (c->phase != kIdle && c->phase != kStaging)
     return fail(c, AFD_ERR_STATE, "the previous exchange is not collected yet");
   if (c->staged[source]) return fail(c, AFD_ERR_STATE, "source %d already dispatched", source);
+  if (c->phase == kStaging && c->cached)
+    return fail(c, AFD_ERR_STATE, "this exchange reuses the last routing (cached dispatch)");
   if (read_host_counts != 0 && read_host_counts != 1)
     return fail(c, AFD_ERR_ARG, "read_host_counts must be 0 or 1");
   if (bucket < 0 || bucket > g.capacity)
@@ -396,46 +458,63 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
   c->rhc = read_host_counts;
 
   if (c->staged_n == g.num_sources) {
-    DispatchParams p;
-    memset(&p, 0, sizeof p);
-    int tok = 0, chunks = 0;
-    for (int s = 0; s < g.num_sources; ++s) {
-      p.src[s] = c->src[s];
-      p.src[s].tok_off = tok;
-      p.src[s].chunk_off = chunks;
-      c->src[s].tok_off = tok;
-      c->src[s].chunk_off = chunks;
-      tok += c->src[s].T;
-      chunks += (c->src[s].T + afd::kChunk - 1) / afd::kChunk;
-    }
-    p.A = g.num_sources;
-    p.F = g.num_workers;
-    p.E = g.num_experts;
-    p.Ef = c->Ef;
-    p.K = g.top_k;
-    p.alpha = g.expert_alignment;
-    p.bucket = bucket;
-    p.row_bytes = c->row_bytes;
-    p.nscale = c->nscale;
-    p.total_tokens = tok;
-    p.total_chunks = chunks;
-    p.R_arena = c->R_arena;
-    p.route_tmp = c->route_tmp;
-    p.chunk_counts = c->chunk_counts;
-    p.chunk_start = c->chunk_start;
-    p.done = c->done;
-    p.err = c->err;
-    p.starts = c->starts;
-    p.ends = c->ends;
-    p.hcounts = c->hcounts;
-    p.routes = c->routes;
-    p.row_src = c->row_src;
-    p.row_w = c->row_w;
-    p.rows = c->rows;
-    p.row_scales = c->row_scales;
-    cudaError_t e = afd::launch_dispatch(p, c->sm_cap, stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "dispatch launch");
-    c->phase = kDispatched;
+    st = launch_exchange_dispatch(c, stream, false);
+    if (st != AFD_OK) return st;
+  }
+  return mark_stream(c, stream);
+}
+
+afd_status afd_source_dispatch_cached(afd_ctx* c, int32_t source, const void* x, const float* weights,
+                                      const float* x_scale, int64_t scale_stride_t,
+                                      int64_t scale_stride_b, int32_t num_tokens, int32_t bucket,
+                                      int32_t read_host_counts, afd_stream stream_) {
+  if (!c) return AFD_ERR_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const afd_config& g = c->cfg;
+  if (source < 0 || source >= g.num_sources) return fail(c, AFD_ERR_ARG, "source %d out of range", source);
+  if (c->phase != kIdle && c->phase != kStaging)
+    return fail(c, AFD_ERR_STATE, "the previous exchange is not collected yet");
+  if (c->staged[source]) return fail(c, AFD_ERR_STATE, "source %d already dispatched", source);
+  if (c->phase == kStaging && !c->cached)
+    return fail(c, AFD_ERR_STATE, "this exchange computes a new layout (afd_source_dispatch)");
+  if (!c->layout_valid) return fail(c, AFD_ERR_STATE, "no earlier layout to reuse");
+  if (bucket != c->layout_bucket || num_tokens != c->layout_T[source])
+    return fail(c, AFD_ERR_STATE, "cached dispatch needs the last layout's num_tokens and bucket");
+  if (read_host_counts != 0 && read_host_counts != 1)
+    return fail(c, AFD_ERR_ARG, "read_host_counts must be 0 or 1");
+  if (c->phase == kStaging && read_host_counts != c->rhc)
+    return fail(c, AFD_ERR_BUCKET, "every role of one exchange passes the same read_host_counts");
+  if (num_tokens > 0) {
+    if (!x) return fail(c, AFD_ERR_ARG, "x is required");
+    if (!aligned16(x)) return fail(c, AFD_ERR_ARG, "x must be 16-byte aligned");
+    if (g.dtype == AFD_FP8_E4M3 && !x_scale) return fail(c, AFD_ERR_ARG, "FP8 dispatch needs x_scale");
+    if (g.dtype == AFD_FP8_E4M3 && (scale_stride_t < 0 || scale_stride_b < 0))
+      return fail(c, AFD_ERR_ARG, "scale strides must be non-negative");
+  }
+  if (read_host_counts && is_capturing(stream))
+    return fail(c, AFD_ERR_CAPTURING, "read_host_counts=1 cannot be captured");
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return fail(c, AFD_ERR_CUDA, "cannot select device %d", c->device);
+  afd_status st = order_stream(c, stream);
+  if (st != AFD_OK) return st;
+
+  SourceDesc& d = c->src[source];
+  d.x = static_cast<const uint8_t*>(x);
+  d.ids = nullptr;
+  d.w = num_tokens > 0 ? weights : nullptr;
+  d.scale = g.dtype == AFD_FP8_E4M3 ? x_scale : nullptr;
+  d.sst = scale_stride_t;
+  d.ssb = scale_stride_b;
+  d.T = num_tokens;
+  c->staged[source] = true;
+  c->staged_n += 1;
+  c->phase = kStaging;
+  c->cached = true;
+  c->bucket = bucket;
+  c->rhc = read_host_counts;
+  if (c->staged_n == g.num_sources) {
+    st = launch_exchange_dispatch(c, stream, true);
+    if (st != AFD_OK) return st;
   }
   return mark_stream(c, stream);
 }

@@ -136,6 +136,25 @@ AFD_API afd_status afd_source_dispatch(afd_ctx* ctx, int32_t source, const void*
                                int32_t num_tokens, int32_t bucket, int32_t read_host_counts,
                                afd_stream stream);
 
+/* Dispatch that reuses the routing of the last exchange (its IDs, layout and
+ * receipts) and moves only the rows: the decode-time routing reuse of
+ * "DeepEP V2 ElasticBuffer first principles", section 4 (cached dispatch
+ * skips the layout and any host synchronization). Every source of the
+ * exchange must use this call (no mixing with afd_source_dispatch), with the
+ * same num_tokens and bucket as in the last exchange whose dispatch ran the
+ * layout; ends[], host counts, row_src and the receipts stay as they were.
+ *   x, x_scale, strides, read_host_counts: as in afd_source_dispatch
+ *   weights    device FP32 [num_tokens, K] new routing weights for the same
+ *              IDs, or NULL to keep the previous exchange's weights
+ * Errors: AFD_ERR_STATE (no layout to reuse, a different num_tokens/bucket,
+ * or an exchange that mixes the two dispatch calls), plus those of
+ * afd_source_dispatch. */
+AFD_API afd_status afd_source_dispatch_cached(afd_ctx* ctx, int32_t source, const void* x,
+                                              const float* weights, const float* x_scale,
+                                              int64_t scale_stride_t, int64_t scale_stride_b,
+                                              int32_t num_tokens, int32_t bucket,
+                                              int32_t read_host_counts, afd_stream stream);
+
 /* What a worker receives. Rows of local expert l (0 <= l < E/F) are
  * [align_up(ends[l-1], alpha), ends[l]) with ends[-1] = 0 ("API contract",
  * Roles and tensors). Inside an expert, rows follow source ascending, then
