@@ -19,6 +19,9 @@ What each function follows (afdEP-comm pages):
 * ``combine``   -- "API contract" (source_collect: BF16 [T,H], summed over the
   selected experts in token order, weight applied once) and design page
   section 19 (FP32 sum in slot order, one rounding to BF16).
+* ``combine_two_stage`` -- design page sections 6 and 19: per-worker BF16
+  partials (optionally E4M3 with a power-of-two scale per 128 elements),
+  summed in FP32 in the order of each worker's last route, rounded once.
 
 Parity pins for each of these live in ``tests/test_oracle_*.py``.
 """
@@ -87,6 +90,9 @@ class Oracle:
             "orc_dispatch": [P, v, v, v, v, v, v, i64, v, v, v, v, v],
             "orc_expert": [P, ctypes.c_int32, v, v, i64, v, v, v],
             "orc_combine": [P, v, v, v, i64, v, v],
+            "orc_float_to_e4m3_n": [v, v, i64],
+            "orc_group_exponent_n": [v, v, i64],
+            "orc_combine_two_stage": [P, v, v, v, i64, v, ctypes.c_int32, v],
         }
         for name, args in sig.items():
             fn = getattr(self.lib, name)
@@ -104,6 +110,18 @@ class Oracle:
         f = np.ascontiguousarray(f, dtype=np.float32)
         out = np.empty(f.shape, np.uint16)
         self.lib.orc_float_to_bf16_n(_ptr(f), _ptr(out), f.size)
+        return out
+
+    def float_to_e4m3(self, f: np.ndarray) -> np.ndarray:
+        f = np.ascontiguousarray(f, dtype=np.float32)
+        out = np.empty(f.shape, np.uint8)
+        self.lib.orc_float_to_e4m3_n(_ptr(f), _ptr(out), f.size)
+        return out
+
+    def group_exponent(self, amax: np.ndarray) -> np.ndarray:
+        amax = np.ascontiguousarray(amax, dtype=np.float32)
+        out = np.empty(amax.shape, np.int32)
+        self.lib.orc_group_exponent_n(_ptr(amax), _ptr(out), amax.size)
         return out
 
     def e4m3_to_float(self, q: np.ndarray) -> np.ndarray:
@@ -221,8 +239,24 @@ def combine(p: Problem, ids, w, slot, r_stride: int, reply: np.ndarray,
     return out
 
 
+COMBINE_FUSED, COMBINE_TWO_STAGE, COMBINE_TWO_STAGE_FP8 = 0, 1, 2
+
+
+def combine_two_stage(p: Problem, ids, w, slot, r_stride: int, reply: np.ndarray, fp8: bool,
+                      orc: Optional[Oracle] = None) -> np.ndarray:
+    """Two-stage combine (per-worker BF16 partials, optionally FP8) -> BF16 bits."""
+    orc = orc or get()
+    out = np.zeros((p.A, p.bucket, p.H), np.uint16)
+    pc = p._c()
+    orc.lib.orc_combine_two_stage(ctypes.byref(pc), _ptr(np.ascontiguousarray(ids, np.int64)),
+                                  _ptr(np.ascontiguousarray(w, np.float32)),
+                                  _ptr(np.ascontiguousarray(slot)), r_stride,
+                                  _ptr(np.ascontiguousarray(reply)), int(bool(fp8)), _ptr(out))
+    return out
+
+
 def round_trip(p: Problem, ids, w, x, x_scales=None, expert_mode: int = EXPERT_IDENTITY,
-               orc: Optional[Oracle] = None) -> dict:
+               orc: Optional[Oracle] = None, combine_mode: int = COMBINE_FUSED) -> dict:
     """validate -> layout -> dispatch -> expert -> combine, all on the CPU."""
     orc = orc or get()
     err = validate(p, ids, orc)
@@ -230,5 +264,9 @@ def round_trip(p: Problem, ids, w, x, x_scales=None, expert_mode: int = EXPERT_I
     r_stride = max(1, int(lay["r_exact"].max()))
     d = dispatch(p, ids, w, x, x_scales, lay, r_stride, orc)
     reply = expert(p, expert_mode, lay, r_stride, d["rows"], d["row_scales"], orc)
-    out = combine(p, ids, w, d["slot"], r_stride, reply, orc)
+    if combine_mode == COMBINE_FUSED:
+        out = combine(p, ids, w, d["slot"], r_stride, reply, orc)
+    else:
+        out = combine_two_stage(p, ids, w, d["slot"], r_stride, reply,
+                                combine_mode == COMBINE_TWO_STAGE_FP8, orc)
     return dict(err=err, r_stride=r_stride, reply=reply, out=out, **lay, **d)

@@ -248,3 +248,111 @@ void orc_float_to_bf16_n(const float* in, uint16_t* out, int64_t n) {
 void orc_e4m3_to_float_n(const uint8_t* in, float* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_to_float(in[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Two-stage combine with optional FP8 partials                              */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3 from the format definition: codes 0..7 are the subnormals m * 2^-9,
+ * code (e+7)*8 + m for e in [-6, 8] is (1 + m/8) * 2^e, 0x7e = 448 is the
+ * largest finite value and 0x7f is NaN. Rounding is to the nearest value,
+ * ties to the even code; anything at or beyond 448 after rounding saturates
+ * to 448. */
+uint8_t orc_float_to_e4m3(float f) {
+  if (isnan(f)) return 0x7f;
+  uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  double a = fabs((double)f); /* exact: float -> double */
+  if (a >= 448.0) return sign | 0x7e;
+  int code;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: quantum 2^-9, codes 0..8 (8 = smallest normal) */
+    double q = a / ldexp(1.0, -9);
+    double n = floor(q);
+    double r = q - n;
+    if (r > 0.5 || (r == 0.5 && fmod(n, 2.0) == 1.0)) n += 1.0;
+    code = (int)n;
+  } else {
+    int e;
+    frexp(a, &e); /* a = m * 2^e with m in [0.5, 1) */
+    e -= 1;       /* now a = (1 + f) * 2^e */
+    double q = a / ldexp(1.0, e - 3); /* in [8, 16) */
+    double n = floor(q);
+    double r = q - n;
+    if (r > 0.5 || (r == 0.5 && fmod(n, 2.0) == 1.0)) n += 1.0;
+    if (n == 16.0) {
+      n = 8.0;
+      e += 1;
+    }
+    code = (e + 7) * 8 + ((int)n - 8);
+    if (code > 0x7e) code = 0x7e; /* the NaN pattern is not a value: saturate */
+  }
+  return (uint8_t)(sign | code);
+}
+
+void orc_float_to_e4m3_n(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_float_to_e4m3(in[i]);
+}
+
+int32_t orc_group_exponent(float amax) {
+  /* the page's definition, searched directly: the first e from -117 up with
+   * amax <= 448 * 2^e evaluated in FP32 (2^e scales exactly; 448 * 2^121 and
+   * above overflow to infinity, so an infinite amax stops at 120) */
+  for (int e = -117; e <= 128; ++e)
+    if (amax <= ldexpf(448.0f, e)) return e;
+  return 128; /* NaN: no e satisfies the comparison */
+}
+
+void orc_group_exponent_n(const float* amax, int32_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_group_exponent(amax[i]);
+}
+
+void orc_combine_two_stage(const orc_problem* p, const int64_t* ids, const float* w,
+                           const int32_t* slot, int64_t r_stride, const uint16_t* reply,
+                           int32_t fp8, uint16_t* out) {
+  const int Ef = p->E / p->F;
+  const int H = p->H;
+  float* acc = (float*)malloc(sizeof(float) * (size_t)H);
+  float* part = (float*)malloc(sizeof(float) * (size_t)H);
+  for (int s = 0; s < p->A; ++s)
+    for (int t = 0; t < p->T[s]; ++t) {
+      for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+      for (int k = 0; k < p->K; ++k) {
+        int64_t rk = route_index(p, s, t, k);
+        if (slot[rk] < 0) continue;
+        int f = (int)(ids[rk] / Ef);
+        /* is k this worker's last route of the token? */
+        int last = 1;
+        for (int j = k + 1; j < p->K; ++j) {
+          int64_t rj = route_index(p, s, t, j);
+          if (slot[rj] >= 0 && (int)(ids[rj] / Ef) == f) last = 0;
+        }
+        if (!last) continue;
+        /* the worker's BF16 partial */
+        for (int h = 0; h < H; ++h) {
+          float a = 0.0f;
+          for (int j = 0; j <= k; ++j) {
+            int64_t rj = route_index(p, s, t, j);
+            if (slot[rj] < 0 || (int)(ids[rj] / Ef) != f) continue;
+            a = fmaf(w[rj], orc_bf16_to_float(reply[(f * r_stride + slot[rj]) * H + h]), a);
+          }
+          part[h] = orc_bf16_to_float(orc_float_to_bf16(a));
+        }
+        if (fp8) {
+          for (int g = 0; g < H / 128; ++g) {
+            float amax = 0.0f;
+            for (int h = g * 128; h < (g + 1) * 128; ++h) amax = fmaxf(amax, fabsf(part[h]));
+            int e = orc_group_exponent(amax);
+            for (int h = g * 128; h < (g + 1) * 128; ++h) {
+              uint8_t q = orc_float_to_e4m3(ldexpf(part[h], -e));
+              part[h] = ldexpf(orc_e4m3_to_float(q), e);
+            }
+          }
+        }
+        for (int h = 0; h < H; ++h) acc[h] = acc[h] + part[h];
+      }
+      for (int h = 0; h < H; ++h)
+        out[((int64_t)s * p->bucket + t) * H + h] = orc_float_to_bf16(acc[h]);
+    }
+  free(acc);
+  free(part);
+}

@@ -86,6 +86,27 @@ void orc_expert(const orc_problem* p, int32_t mode, const int32_t* start,
                 const int32_t* ends, int64_t r_stride, const uint8_t* rows,
                 const float* row_scales, uint16_t* reply);
 
+/* OCP E4M3 encoding, round to nearest even, saturating: finite values beyond
+ * 448 and infinities become +-448; NaN becomes S.1111.111. */
+uint8_t orc_float_to_e4m3(float f);
+void orc_float_to_e4m3_n(const float* in, uint8_t* out, int64_t n);
+
+/* Power-of-two scale exponent of one 128-element group (design page,
+ * "19. FP8 combine replies"): the smallest integer e with amax <= 448 * 2^e,
+ * compared in FP32, and at least -117. */
+int32_t orc_group_exponent(float amax);
+void orc_group_exponent_n(const float* amax, int32_t* out, int64_t n);
+
+/* Two-stage combine (design page, sections 6 and 19): for every token, each
+ * worker's routes give a BF16 partial (FP32 fused multiply-adds in ascending
+ * k from +0, one rounding); with fp8 != 0 each partial is quantized to E4M3
+ * with one power-of-two scale per 128 elements and dequantized; the partials
+ * are added in FP32 in the order of each worker's last route (ascending k),
+ * from +0, and the sum is rounded once to BF16. */
+void orc_combine_two_stage(const orc_problem* p, const int64_t* ids, const float* w,
+                           const int32_t* slot, int64_t r_stride, const uint16_t* reply,
+                           int32_t fp8, uint16_t* out);
+
 /* out[s][t][h] = bf16( fma chain over k ascending of w[s][t][k] *
  * reply[f][slot][h] ), starting from +0.0f; skipped routes add nothing.
  * out is [A][bucket][H]; rows t >= T[s] are left untouched. */
