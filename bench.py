@@ -477,7 +477,8 @@ def measure_e2e(torch, buf, wl, inp, dev, steps: int, flush):
 
 def measure_sweep(torch, afd, W, config, dev, flush):
     """Graph-replayed round trip at the workload's other token counts
-    (L2 flushed before each replay)."""
+    (L2 flushed before each replay), with a full dispatch and with a cached
+    dispatch (the last exchange's routing reused)."""
     out = {}
     table = {"2A2F": (1, 8, 32, 128, 512, 2048), "2A2F-H4096": (1, 128, 2048)}
     for name, Ts in (("2A2F", table["2A2F"]), ("2A2F-H4096", table["2A2F-H4096"])):
@@ -500,25 +501,35 @@ def measure_sweep(torch, afd, W, config, dev, flush):
                 for s in range(wl.A):
                     buf.source_collect(s, out=outs[s])
 
-            exchange()
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                exchange()
-            for _ in range(3):
-                g.replay()
-            times = []
-            for _ in range(10):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                g.replay()
-                b.record()
-                b.synchronize()
-                times.append(a.elapsed_time(b) * 1e3)
-            del g
+            def exchange_cached():
+                for s in range(wl.A):
+                    buf.source_dispatch_cached(s, xs[s], ws_[s], bucket=wl.bucket)
+                for f in range(wl.F):
+                    r = buf.worker_receive(f, bucket=wl.bucket)
+                    buf.worker_reply(f, r.rows, r.receipt)
+                for s in range(wl.A):
+                    buf.source_collect(s, out=outs[s])
+
+            for label, fn in (("", exchange), (" cached", exchange_cached)):
+                fn()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                for _ in range(3):
+                    g.replay()
+                times = []
+                for _ in range(10):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    g.replay()
+                    b.record()
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) * 1e3)
+                del g
+                out[f"{name} T={T}{label}"] = round(statistics.median(times), 2)
             buf.close()
-            out[f"{name} T={T}"] = round(statistics.median(times), 2)
     return out
 
 

@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libafd.so")
 OK, ERR_ARG, ERR_STATE, ERR_BUCKET, ERR_RECEIPT = 0, 1, 2, 3, 4
 ERR_ROUTE_RANGE, ERR_ROUTE_DUP, ERR_CUDA, ERR_OOM, ERR_CAPTURING, ERR_UNSUPPORTED = 5, 6, 7, 8, 9, 10
 BF16, FP8_E4M3 = 0, 1
+COMBINE_FUSED, COMBINE_TWO_STAGE, COMBINE_TWO_STAGE_FP8 = 0, 1, 2
 
 EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispatch_cached",
            "afd_worker_receive",
@@ -43,7 +44,7 @@ class AfdError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_sources", "num_workers", "num_experts", "top_k", "hidden", "capacity",
-        "expert_alignment", "dtype", "num_sms")]
+        "expert_alignment", "dtype", "num_sms", "combine_mode")]
 
 
 class Recv(ctypes.Structure):
@@ -166,12 +167,13 @@ class Buffer:
 
     def __init__(self, num_sources: int, num_workers: int, num_experts: int, top_k: int,
                  hidden: int, capacity: int, expert_alignment: int = 1, dtype: str = "bf16",
-                 num_sms: int = 0, device=None):
+                 num_sms: int = 0, device=None, combine_mode: int = COMBINE_FUSED):
         self._lib = load_library()
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         self.cfg = Config(num_sources, num_workers, num_experts, top_k, hidden, capacity,
-                          expert_alignment, FP8_E4M3 if dtype == "fp8" else BF16, num_sms)
+                          expert_alignment, FP8_E4M3 if dtype == "fp8" else BF16, num_sms,
+                          combine_mode)
         self.dtype = dtype
         self.A, self.F, self.E, self.K, self.H = num_sources, num_workers, num_experts, top_k, hidden
         self.Ef = num_experts // max(num_workers, 1)

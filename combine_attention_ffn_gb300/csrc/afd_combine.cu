@@ -17,6 +17,7 @@
 // spreads few-token combines the same way) and balances large batches.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -178,6 +179,118 @@ __global__ void __launch_bounds__(64) combine_token_kernel(const __grid_constant
   }
 }
 
+// ---- two-stage combine (optionally with E4M3 partials) ----
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// 2^e as an FP32 value (e in [-126, 127]).
+__device__ __forceinline__ float exp2_int(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// The smallest integer e >= -117 with amax <= 448 * 2^e, from amax's FP32
+// bits: amax = (1 + m) * 2^E fits under 1.75 * 2^(E) exactly when m <= 0.75.
+// An infinite amax gives 120; zero or subnormal amax gives -117.
+__device__ __forceinline__ int group_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int E = (int)((b >> 23) & 0xffu);
+  if (E == 0) return -117;
+  int e = (E - 127) - 8 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  return e < -117 ? -117 : e;
+}
+
+// Rounds v to E4M3 (nearest even, saturating) and back, exactly as the
+// conversion instructions do.
+__device__ __forceinline__ void e4m3_round_trip2(float& a, float& b) {
+  uint16_t q;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(a), "f"(b));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  a = __high2float(hv);
+  b = __low2float(hv);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_constant__ CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;  // <= kGroup
+  const int nseg = p.H >> 8;
+  const int64_t items = (int64_t)p.total_tokens * nseg;
+
+  for (int64_t it = gwarp; it < items; it += nwarps) {
+    const int gt = (int)(it / nseg);
+    const int seg = (int)(it - (int64_t)gt * nseg);
+    const int s = source_of(p, gt);
+    const int t = gt - p.tok_off[s];
+    int2 r = make_int2(-1, 0);
+    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    const int v = seg * 32 + lane;
+
+    uint4 buf[kGroup];
+    float wk[kGroup];
+    int wf[kGroup];  // worker of each valid route, -1 otherwise
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const int c = __shfl_sync(0xffffffffu, r.x, j);
+      wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
+      wf[j] = (j < K && c >= 0) ? (c >> kWorkerShift) : -1;
+      if (wf[j] >= 0)
+        buf[j] = ld_once(reinterpret_cast<const uint4*>(p.reply[wf[j]] + (int64_t)(c & kRowMask) * p.H) + v);
+    }
+
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) {
+      if (wf[k] < 0) continue;
+      bool last = true;
+#pragma unroll
+      for (int j = k + 1; j < kGroup; ++j) last = last && (wf[j] != wf[k]);
+      if (!last) continue;
+      // this worker's partial: its routes in ascending k, one BF16 rounding
+      float part[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part[e] = 0.0f;
+#pragma unroll
+      for (int j = 0; j <= k; ++j)
+        if (wf[j] == wf[k]) fma8(part, wk[j], buf[j]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part[e] = bf16_round(part[e]);
+      if (kFp8) {
+        // one power-of-two scale per 128 elements: 16 lanes x 8 elements
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(part[e]));
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        const int ge = group_exponent(amax);
+        const float down = exp2_int(-ge), up = exp2_int(ge);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          float a = part[e] * down, b = part[e + 1] * down;
+          e4m3_round_trip2(a, b);
+          part[e] = a * up;
+          part[e + 1] = b * up;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = acc[e] + part[e];
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s])[v] = o;
+  }
+}
+
 __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -213,6 +326,13 @@ cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stre
 // stream and wait for it before reading anything.
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
   if (p.total_tokens <= 0) return cudaSuccess;
+  if (p.mode != 0) {
+    const int64_t items = (int64_t)p.total_tokens * (p.H >> 8);
+    int64_t grid = (items + 7) / 8;
+    if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
+    return p.mode == 2 ? launch_pdl(combine_two_stage_kernel<true>, grid, 256, stream, p)
+                       : launch_pdl(combine_two_stage_kernel<false>, grid, 256, stream, p);
+  }
   if (p.K <= kGroup && p.total_tokens >= sm_cap * AFD_TOKEN_COMBINE_MIN) {
     // enough tokens for a warp each on every SM: the pipelined per-token
     // kernel, in two-warp blocks so that tokens spread evenly over the SMs

@@ -84,6 +84,7 @@ struct CombineParams {
   int32_t tok_off[kMaxSources];      // first flattened token of each source in this launch
   const uint16_t* reply[kMaxWorkers];// BF16 [rows][H] per worker
   int32_t A, K, H, total_tokens;
+  int32_t mode;                      // AFD_COMBINE_*
 };
 
 struct CopyParams {

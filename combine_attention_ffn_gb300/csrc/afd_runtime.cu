@@ -218,6 +218,10 @@ afd_status check_config(const afd_config* g, afd_ctx* c) {
   if (g->dtype != AFD_BF16 && g->dtype != AFD_FP8_E4M3)
     return fail(c, AFD_ERR_ARG, "dtype must be AFD_BF16 or AFD_FP8_E4M3");
   if (g->num_sms < 0) return fail(c, AFD_ERR_ARG, "num_sms must be >= 0");
+  if (g->combine_mode < AFD_COMBINE_FUSED || g->combine_mode > AFD_COMBINE_TWO_STAGE_FP8)
+    return fail(c, AFD_ERR_ARG, "unknown combine_mode");
+  if (g->combine_mode != AFD_COMBINE_FUSED && g->top_k > 8)
+    return fail(c, AFD_ERR_UNSUPPORTED, "the two-stage combine modes need top_k <= 8");
   return AFD_OK;
 }
 
@@ -611,6 +615,7 @@ afd_status afd_worker_reply(afd_ctx* c, int32_t worker, const void* rows, int64_
         tok += c->src[s].T;
       }
       p.reply[0] = c->reply[0];
+      p.mode = g.combine_mode;
       p.A = g.num_sources;
       p.K = g.top_k;
       p.H = g.hidden;
@@ -664,6 +669,7 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
     p.out_stride[0] = g.hidden;
     p.tok_off[0] = 0;
     for (int f = 0; f < g.num_workers; ++f) p.reply[f] = c->reply[f];
+    p.mode = g.combine_mode;
     p.A = 1;
     p.K = g.top_k;
     p.H = g.hidden;

@@ -76,6 +76,20 @@ typedef enum afd_status {
 
 enum { AFD_BF16 = 0, AFD_FP8_E4M3 = 1 };
 
+/* How the combine sums a token's reply rows (afd_config.combine_mode).
+ * FUSED: one FP32 fused multiply-add chain over the routes in ascending k,
+ *   one rounding to BF16.
+ * TWO_STAGE: the pages' two-stage reduction (afdEP-comm design page,
+ *   sections 6 and 19): each worker's routes give a BF16 partial (FMA chain
+ *   in ascending k, one rounding); the partials are added in FP32 in the
+ *   order of each worker's last route and rounded once. Equal to FUSED when
+ *   F == 1.
+ * TWO_STAGE_FP8: as TWO_STAGE, with each partial carried as E4M3 with one
+ *   power-of-two scale 2^e per 128 elements (e the smallest integer >= -117
+ *   with amax <= 448 * 2^e), the lossy reply format of section 19.
+ * The two-stage modes need top_k <= 8. */
+enum { AFD_COMBINE_FUSED = 0, AFD_COMBINE_TWO_STAGE = 1, AFD_COMBINE_TWO_STAGE_FP8 = 2 };
+
 /* Fixed per context. "API contract", Roles and tensors: H is a multiple of
  * 256, K <= min(32, E), experts divide evenly over the workers (worker f owns
  * experts [f*E/F, (f+1)*E/F)). Limits of this build: A <= 64, F <= 64,
@@ -90,6 +104,7 @@ typedef struct afd_config {
   int32_t expert_alignment; /* alpha >= 1: each expert's first row is a multiple of alpha */
   int32_t dtype;            /* AFD_BF16, or AFD_FP8_E4M3 (E4M3 rows + FP32 block-128 scales) */
   int32_t num_sms;          /* cap on the SMs the kernels spread over; 0 = every SM */
+  int32_t combine_mode;     /* AFD_COMBINE_FUSED (0), _TWO_STAGE or _TWO_STAGE_FP8 */
 } afd_config;
 
 /* Creates a context on `device` and allocates its device arenas:

@@ -20,8 +20,9 @@ from combine_attention_ffn_gb300 import workloads as W
 IDENTITY, SCALE = oracle.EXPERT_IDENTITY, oracle.EXPERT_SCALE
 
 
-def make_buffer(wl: W.Workload, num_sms: int = 0) -> afd.Buffer:
-    return afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype, num_sms)
+def make_buffer(wl: W.Workload, num_sms: int = 0, combine_mode: int = 0) -> afd.Buffer:
+    return afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype, num_sms,
+                      combine_mode=combine_mode)
 
 
 @dataclass
@@ -131,11 +132,12 @@ def snapshot(recvs) -> dict:
     return snap
 
 
-def expected(inp: W.Inputs, mode: int) -> dict:
+def expected(inp: W.Inputs, mode: int, combine_mode: int = 0) -> dict:
     wl = inp.wl
     p = oracle.Problem(wl.A, wl.F, wl.E, wl.K, wl.H, wl.alpha, wl.bucket,
                        oracle.FP8 if wl.dtype == "fp8" else oracle.BF16, list(wl.T))
-    r = oracle.round_trip(p, inp.ids, inp.w, inp.x, inp.x_scales, expert_mode=mode)
+    r = oracle.round_trip(p, inp.ids, inp.w, inp.x, inp.x_scales, expert_mode=mode,
+                          combine_mode=combine_mode)
     return r
 
 
