@@ -519,6 +519,99 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) cached_scatter_kernel(const
   }
 }
 
+// ---------------------------------------------------------------- tiny path
+
+// At most 32 tokens in the whole exchange: one-warp blocks. Every block
+// counts all the routes itself with one lane mask per expert (lane = token),
+// so ranks are popcounts of earlier lanes and no block-wide barrier is
+// needed; block b < N then scatters token b, and all blocks share the padding
+// rows.
+__global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant__ DispatchParams p) {
+  extern __shared__ __align__(16) uint32_t tsm[];
+  const int E = p.E, K = p.K, N = p.total_tokens;
+  uint32_t* mask = tsm;                                     // [E]
+  int32_t* sh_start = reinterpret_cast<int32_t*>(mask + E);  // [E]
+  int32_t* sh_end = sh_start + E;                           // [E]
+  pdl_launch_dependents();
+  const int lane = threadIdx.x;
+
+  uint4 pre[kScatterVecs];
+  float pre_w = 0.0f;
+  const bool has_token = preload_first(p, blockIdx.x, pre, pre_w);  // token blockIdx.x, if any
+
+  for (int e = lane; e < E; e += 32) mask[e] = 0u;
+  __syncwarp();
+  uint32_t valid = 0u;
+  if (lane < N) {
+    const int s = source_of_token(p, lane);
+    const int t = lane - p.src[s].tok_off;
+    valid = mark_token(p.src[s].ids + (int64_t)t * K, K, E, mask, lane, s, t,
+                       blockIdx.x == 0 ? p.err : nullptr);
+  }
+  __syncwarp();
+  // aligned scan per worker, one warp
+  for (int f = 0; f < p.F; ++f) {
+    int carry = 0;
+    for (int l0 = 0; l0 < p.Ef; l0 += 32) {
+      const int l = l0 + lane;
+      const int e = f * p.Ef + l;
+      const int cnt = l < p.Ef ? __popc(mask[e]) : 0;
+      const int al = align_up_dev(cnt, p.alpha);
+      const int incl = warp_inclusive_scan(al);
+      if (l < p.Ef) {
+        const int start = carry + incl - al;
+        sh_start[e] = start;
+        sh_end[e] = start + cnt;
+        if (blockIdx.x == 0) {
+          p.starts[e] = start;
+          p.ends[e] = start + cnt;
+          p.hcounts[e] = al;
+        }
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncwarp();
+
+  auto row_of = [&](int gt, int s, int t, int& e, int& row) -> bool {
+    if (!((__shfl_sync(0xffffffffu, valid, gt) >> lane) & 1u)) return false;
+    e = (int)p.src[s].ids[(int64_t)t * K + lane];
+    row = sh_start[e] + __popc(mask[e] & ((1u << gt) - 1u));
+    return true;
+  };
+  // the route rows of one token; all 32 lanes take part (the valid mask is
+  // gathered with a shuffle), lanes >= K only copy
+  const int gt = blockIdx.x;
+  if (has_token) {
+    const int s = source_of_token(p, gt);
+    const SourceDesc& src = p.src[s];
+    const int t = gt - src.tok_off;
+    int e = -1, row = 0;
+    const bool ok = row_of(gt, s, t, e, row);
+    int code = -1;
+    if (lane < K) {
+      if (ok) {
+        code = write_route(p, s, t, gt, e, row, pre_w);
+      } else {
+        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+      }
+    }
+    copy_token<true>(p, src, t, code, pre);
+  }
+  // padding rows, spread over the blocks
+  if (p.alpha > 1) {
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+      const int end = sh_end[e];
+      const int lim = align_up_dev(end, p.alpha);
+      const int64_t base = (int64_t)(e / p.Ef) * p.R_arena;
+      for (int row = end + lane; row < lim; row += 32) {
+        p.row_src[base + row] = -1;
+        p.row_w[base + row] = 0.0f;
+      }
+    }
+  }
+}
+
 size_t layout_smem(int E) {
   const size_t count = (size_t)kChunkWarps * E * (sizeof(uint32_t) + sizeof(uint16_t));
   const size_t finish = (size_t)(kChunk + 2 * E) * sizeof(int32_t);
@@ -568,6 +661,11 @@ cudaError_t configure_dispatch_kernels() {
 // exchange's combine, which still reads the arenas it overwrites.
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   const int block = 256;
+  if (p.total_tokens >= 1 && p.total_tokens <= 32 && AFD_TINY_DISPATCH) {
+    // one block per token, and at least 16 blocks to share the padding rows
+    const int grid = p.total_tokens > 16 ? p.total_tokens : 16;
+    return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, false, p);
+  }
   if (dispatch_is_small(p)) {
     int grid = (p.total_tokens + 7) / 8;
     if (grid > sm_cap) grid = sm_cap;

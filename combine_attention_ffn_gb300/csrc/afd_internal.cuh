@@ -23,6 +23,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_SCATTER_BLOCK
 #define AFD_SCATTER_BLOCK 128    // threads per scatter block (a warp per token)
 #endif
+#ifndef AFD_TINY_DISPATCH
+#define AFD_TINY_DISPATCH 1       // exchanges of at most 32 tokens take the one-warp dispatch
+#endif
 #ifndef AFD_TOKEN_COMBINE_MIN
 #define AFD_TOKEN_COMBINE_MIN 8  // x SMs: tokens from which the per-token combine is used
 #endif

@@ -29,25 +29,27 @@ def _oracle_first_error(inp):
     return {0: 0, oracle.ROUTE_RANGE: afd.ERR_ROUTE_RANGE, oracle.ROUTE_DUP: afd.ERR_ROUTE_DUP}[code], s, t, k
 
 
+@pytest.mark.parametrize("T", [300, 100, 8])
 @pytest.mark.parametrize("plant", ["range_high", "range_low", "wide", "dup", "two_errors",
                                    "dup_and_range_later"])
-def test_invalid_routes_reported_like_the_oracle(plant):
-    wl = W.named("2A2F", T=300)
+def test_invalid_routes_reported_like_the_oracle(plant, T):
+    wl = W.named("2A2F", T=T)
     inp = W.make_inputs(wl)
+    at = lambda t: t * T // 300  # the same relative positions at every size
     if plant == "range_high":
-        inp.ids[1, 123, 4] = 128
+        inp.ids[1, at(123), 4] = 128
     elif plant == "range_low":
-        inp.ids[0, 299, 7] = -5
+        inp.ids[0, at(299), 7] = -5
     elif plant == "wide":
         inp.ids[1, 0, 0] = (1 << 33) + 3   # 3 if truncated to 32 bits
     elif plant == "dup":
-        inp.ids[0, 77, 6] = inp.ids[0, 77, 2]
+        inp.ids[0, at(77), 6] = inp.ids[0, at(77), 2]
     elif plant == "two_errors":
-        inp.ids[1, 5, 1] = 999
-        inp.ids[0, 260, 3] = inp.ids[0, 260, 0]
+        inp.ids[1, at(5), 1] = 999
+        inp.ids[0, at(260), 3] = inp.ids[0, at(260), 0]
     elif plant == "dup_and_range_later":
-        inp.ids[0, 10, 5] = inp.ids[0, 10, 4]
-        inp.ids[0, 10, 6] = 4000
+        inp.ids[0, at(10), 5] = inp.ids[0, at(10), 4]
+        inp.ids[0, at(10), 6] = 4000
     want = _oracle_first_error(inp)
     assert want[0] != 0
     buf = GH.make_buffer(wl)
@@ -56,7 +58,7 @@ def test_invalid_routes_reported_like_the_oracle(plant):
         GH.run_exchange(buf, wl, dev)
         assert buf.get_error() == want
         # sticky across an exchange with valid routes
-        good = W.make_inputs(W.named("2A2F", T=300))
+        good = W.make_inputs(W.named("2A2F", T=T))
         GH.run_exchange(buf, wl, GH.to_device(good))
         assert buf.get_error() == want
         buf.clear_error()
