@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--under-load", action="store_true",
+                    help="time the exchange and a side-stream GEMM batch alone and together "
+                         "(the pages' synthetic compute load) and print that record instead")
     ap.add_argument("--profile-exchanges", type=int, default=0,
                     help="run this many eager exchanges of the workload and exit "
                          "(a short, untimed program for an external profiler)")
@@ -231,10 +234,113 @@ def workload_config(wl, execution: str = "one CUDA graph per round trip",
 
 
 # ------------------------------------------------------------------ our arm
+def run_under_load(args):
+    """The exchange under compute load (afdEP-comm design page, section 14:
+    a fixed batch of 2,048^3 BF16 GEMMs on a side stream while the exchanges
+    replay). For each token count and SM cap: GEMM time alone and under the
+    exchange, exchange time alone and under the GEMMs, and the makespan."""
+    import torch
+
+    from combine_attention_ffn_gb300 import afd
+    from combine_attention_ffn_gb300 import build as libbuild
+    from combine_attention_ffn_gb300 import workloads as W
+
+    libbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    side_s = torch.cuda.Stream()
+    a = torch.randn(2048, 2048, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(2048, 2048, device=dev, dtype=torch.bfloat16)
+    c = torch.empty(2048, 2048, device=dev, dtype=torch.bfloat16)
+    n_ex, n_gemm = 200, 200
+
+    main_s = torch.cuda.current_stream()
+
+    def span(fn_main, fn_side):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda.synchronize()
+        e[0].record(main_s)
+        side_s.wait_event(e[0])
+        if fn_side:
+            with torch.cuda.stream(side_s):
+                e[2].record(side_s)
+                fn_side()
+                e[3].record(side_s)
+        if fn_main:
+            fn_main()
+        e[1].record(main_s)
+        torch.cuda.synchronize()
+        t_main = e[0].elapsed_time(e[1]) * 1e3 if fn_main else None
+        t_side = e[2].elapsed_time(e[3]) * 1e3 if fn_side else None
+        make = max(e[0].elapsed_time(e[1]), e[0].elapsed_time(e[3]) if fn_side else 0) * 1e3
+        return t_main, t_side, make
+
+    def gemms():
+        for _ in range(n_gemm):
+            torch.matmul(a, b, out=c)
+
+    rows = []
+    for T in (1, 32, 512, 2048):
+        wl = W.named(args.config, T=T)
+        inp = W.make_inputs(wl)
+        xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+              for s in range(wl.A)]
+        ids = [torch.from_numpy(inp.ids[s, :T].copy()).to(dev) for s in range(wl.A)]
+        ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s in range(wl.A)]
+        outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(wl.A)]
+        for sms, prio in ((0, False), (64, False), (24, False), (0, True)):
+            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype, num_sms=sms)
+            # the exchange's stream: the default one, or one of the highest priority
+            main_s = torch.cuda.Stream(priority=torch.cuda.Stream.priority_range()[1]) if prio \
+                else torch.cuda.default_stream()
+            torch.cuda.set_stream(main_s)
+
+            def exchange():
+                for s in range(wl.A):
+                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
+                for f in range(wl.F):
+                    r = buf.worker_receive(f, bucket=wl.bucket)
+                    buf.worker_reply(f, r.rows, r.receipt)
+                for s in range(wl.A):
+                    buf.source_collect(s, out=outs[s])
+
+            exchange()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                exchange()
+
+            def replays():
+                for _ in range(n_ex):
+                    g.replay()
+
+            span(replays, gemms)  # warm-up
+            ex_alone, _, _ = span(replays, None)
+            _, gemm_alone, _ = span(None, gemms)
+            ex_load, gemm_load, make = span(replays, gemms)
+            rows.append({"T": T, "num_sms": sms, "exchange_stream": "high priority" if prio else "default",
+                         "exchange_us_alone": round(ex_alone / n_ex, 2),
+                         "exchange_us_under_load": round(ex_load / n_ex, 2),
+                         "gemm_us_alone": round(gemm_alone / n_gemm, 2),
+                         "gemm_us_under_load": round(gemm_load / n_gemm, 2),
+                         "gemm_slowdown": round(gemm_load / gemm_alone - 1, 4),
+                         "makespan_ms": round(make / 1e3, 3)})
+            del g
+            buf.close()
+            torch.cuda.set_stream(torch.cuda.default_stream())
+    print(json.dumps({"metric": "exchange and side-stream GEMM under load", "mode": "under_load",
+                      "config": {"workload": args.config, "gemm": "2048^3 BF16 (torch.matmul) x 200",
+                                 "exchanges": n_ex, "execution": "one CUDA graph per exchange"},
+                      "rows": rows}))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.under_load:
+        return run_under_load(args)
 
     import torch
 
