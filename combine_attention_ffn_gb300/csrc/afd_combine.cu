@@ -147,9 +147,15 @@ __global__ void __launch_bounds__(64) combine_token_kernel(const __grid_constant
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int K = p.K;
-  const int nseg = p.H >> 8;
+  // a warp takes 1/split of a token's segments (split divides the count)
+  const int nseg_all = p.H >> 8;
+  const int split = nseg_all % AFD_COMBINE_SPLIT == 0 ? AFD_COMBINE_SPLIT : 1;
+  const int nseg = nseg_all / split;
+  const int items = p.total_tokens * split;
 
-  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
+  for (int item = gwarp; item < items; item += nwarps) {
+    const int gt = item / split;
+    const int seg0 = (item - gt * split) * nseg;
     const int s = source_of(p, gt);
     const int t = gt - p.tok_off[s];
     int2 r = make_int2(-1, 0);
@@ -165,7 +171,9 @@ __global__ void __launch_bounds__(64) combine_token_kernel(const __grid_constant
       okmask |= (ok ? 1u : 0u) << j;
       rowp[j] = ok ? p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
     }
-    uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]);
+    uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]) + seg0 * 32;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
     uint4 a[kGroup], b[kGroup];
     load_seg(a, rowp, okmask, lane);
     int seg = 0;
@@ -336,7 +344,7 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
   if (p.K <= kGroup && p.total_tokens >= sm_cap * AFD_TOKEN_COMBINE_MIN) {
     // enough tokens for a warp each on every SM: the pipelined per-token
     // kernel, in two-warp blocks so that tokens spread evenly over the SMs
-    int64_t grid = (p.total_tokens + 1) / 2;
+    int64_t grid = ((int64_t)p.total_tokens * AFD_COMBINE_SPLIT + 1) / 2;
     if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
     return launch_pdl(combine_token_kernel, grid, 64, stream, p);
   }

@@ -26,6 +26,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_TINY_DISPATCH
 #define AFD_TINY_DISPATCH 1       // exchanges of at most 32 tokens take the one-warp dispatch
 #endif
+#ifndef AFD_COMBINE_SPLIT
+#define AFD_COMBINE_SPLIT 1       // warps per token in the per-token combine
+#endif
 #ifndef AFD_TOKEN_COMBINE_MIN
 #define AFD_TOKEN_COMBINE_MIN 8  // x SMs: tokens from which the per-token combine is used
 #endif
