@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--under-load", action="store_true",
                     help="time the exchange and a side-stream GEMM batch alone and together "
                          "(the pages' synthetic compute load) and print that record instead")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="time every workload at each of its token counts and print that table")
     ap.add_argument("--profile-exchanges", type=int, default=0,
                     help="run this many eager exchanges of the workload and exit "
                          "(a short, untimed program for an external profiler)")
@@ -57,7 +59,7 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
-def algorithmic_bytes(wl, inp) -> dict:
+def algorithmic_bytes(wl, inp, view: bool = False) -> dict:
     """Bytes the exchange must move once (read x, write routed rows, read
     replies, write out) plus its metadata, per phase and per launch."""
     valid = 0
@@ -68,8 +70,24 @@ def algorithmic_bytes(wl, inp) -> dict:
     R_in = wl.row_bytes + (4 * (H // 128) if wl.dtype == "fp8" else 0)
     dispatch = toks * R_in + valid * R_in + toks * K * (8 + 4) + valid * (4 + 4) + toks * K * (4 + 8)
     combine = valid * 2 * H + toks * 2 * H + toks * K * 8
-    return dict(valid=valid, dispatch=dispatch, combine=combine, total=dispatch + combine,
+    # one worker without the view: collect copies the inbox into `out`
+    copy = 2 * toks * 2 * H if (wl.F == 1 and not view) else 0
+    return dict(valid=valid, dispatch=dispatch, combine=combine, copy=copy,
+                total=dispatch + combine + copy,
                 payload=toks * R_in + valid * R_in + valid * 2 * H + toks * 2 * H)
+
+
+def native_digest() -> str:
+    """Hash of the library's sources and header: names the native code a
+    record was measured with."""
+    import glob
+
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "combine_attention_ffn_gb300", "csrc", "*")))
+    for f in files + [os.path.join(ROOT, "include", "afd.h")]:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -217,6 +235,7 @@ def run_reference(args):
         "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle"},
         "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "native_digest": native_digest(),
     }
     print(json.dumps(line))
     return 0
@@ -335,12 +354,136 @@ def run_under_load(args):
     return 0
 
 
+ALL_CONFIGS = (("tiny", (16,)), ("2A2F", (1, 8, 32, 128, 512, 2048)),
+               ("2A2F-H4096", (1, 128, 2048)), ("skew-3A1F", (1, 32, 512, 2048)),
+               ("skew-1A3F", (1, 32, 512, 2048)), ("fp8-2A2F", (1, 128, 2048)),
+               ("fp8-2A1F", (1, 128, 2048)))
+
+
+def run_all_configs(args):
+    """Every workload at each of its token counts, one CUDA graph replay per
+    step, L2 flushed before each replay. BF16: the whole round trip with the
+    identity expert. FP8: the replies need an expert (BF16 from the E4M3 rows
+    and scales), which runs untimed between two graphs: dispatch + receive,
+    then reply + collect; the value is their sum."""
+    import torch
+
+    from combine_attention_ffn_gb300 import afd
+    from combine_attention_ffn_gb300 import build as libbuild
+    from combine_attention_ffn_gb300 import workloads as W
+
+    libbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peak, peak_kind = load_peaks()
+
+    def timed(fn, n=15):
+        times = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(times)
+
+    rows = []
+    for name, Ts in ALL_CONFIGS:
+        for T in Ts:
+            wl = W.named(name, T=T)
+            inp = W.make_inputs(wl)
+            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
+            fp8 = wl.dtype == "fp8"
+            if fp8:
+                xs = [torch.from_numpy(inp.x[s, :t].copy()).to(dev).view(torch.float8_e4m3fn)
+                      for s, t in enumerate(wl.T)]
+                scs = [torch.from_numpy(inp.x_scales[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+            else:
+                xs = [torch.from_numpy(inp.x[s, :t].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+                      for s, t in enumerate(wl.T)]
+                scs = [None] * wl.A
+            ids = [torch.from_numpy(inp.ids[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+            ws_ = [torch.from_numpy(inp.w[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+            outs = [torch.empty((t, wl.H), dtype=torch.bfloat16, device=dev) for t in wl.T]
+            recv = {}
+            replies = {}
+
+            def first_half():
+                for s in range(wl.A):
+                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], scs[s], bucket=wl.bucket)
+                for f in range(wl.F):
+                    recv[f] = buf.worker_receive(f, bucket=wl.bucket)
+
+            def expert():
+                for f in range(wl.F):
+                    r = recv[f]
+                    if fp8:
+                        v = r.rows.float() * r.row_scales.repeat_interleave(128, dim=1)
+                        replies[f] = v.to(torch.bfloat16)
+                    else:
+                        replies[f] = r.rows
+
+            use_view = [False]
+
+            def second_half():
+                for f in range(wl.F):
+                    buf.worker_reply(f, replies[f], recv[f].receipt)
+                for s in range(wl.A):
+                    buf.source_collect(s, out=None if use_view[0] else outs[s], view=use_view[0])
+
+            for use_view[0] in ((False, True) if wl.F == 1 else (False,)):
+                first_half(); expert(); second_half()
+                torch.cuda.synchronize()
+                us = timed_exchange(fp8, first_half, expert, second_half, timed, torch)
+                ab = algorithmic_bytes(wl, inp, view=use_view[0])
+                gbs = ab["total"] / (us * 1e-6) / 1e9
+                rows.append({"config": name + (" view" if use_view[0] else ""), "T": T,
+                             "us": round(us, 2), "gbs": round(gbs, 1),
+                             "frac": round(gbs / peak, 4) if T >= 512 else None})
+            buf.close()
+    print(json.dumps({"metric": METRIC, "mode": "all_configs", "unit": "us", "peak_gbs": peak,
+                      "peak_kind": peak_kind, "native_digest": native_digest(),
+                      "l2": "flushed before every timed replay", "rows": rows}))
+    return 0
+
+
+def timed_exchange(fp8, first_half, expert, second_half, timed, torch):
+    """Graph-replayed exchange time; FP8 sums the two graphs around the expert."""
+    if fp8:
+        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1):
+            first_half()
+        expert()
+        with torch.cuda.graph(g2):
+            second_half()
+        g1.replay()
+        g2.replay()
+        us = timed(g1.replay) + timed(g2.replay)
+        del g1, g2
+    else:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            first_half()
+            expert()
+            second_half()
+        g.replay()
+        us = timed(g.replay)
+        del g
+    torch.cuda.synchronize()
+    return us
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.under_load:
         return run_under_load(args)
+    if args.all_configs:
+        return run_all_configs(args)
 
     import torch
 
@@ -408,6 +551,16 @@ def main():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         exchange()
+    def exchange_batched():
+        dispatch_all()
+        receive_reply_all()
+        buf.source_collect_all(outs=outs)
+
+    exchange_batched()
+    torch.cuda.synchronize()
+    g_batched = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_batched):
+        exchange_batched()
     g_phase = []
     for fn in (dispatch_all, receive_reply_all, collect_all):
         gp = torch.cuda.CUDAGraph()
@@ -438,6 +591,7 @@ def main():
         return torch.cuda.Event(enable_timing=True)
 
     steps_ev = [(ev(), ev()) for _ in range(args.steps)]
+    batched_ev = [(ev(), ev()) for _ in range(args.steps)]
     phase_ev = [[ev() for _ in range(4)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
@@ -454,6 +608,10 @@ def main():
         for j, gp in enumerate(g_phase):
             gp.replay()
             pe[j + 1].record()
+        flush.zero_()
+        batched_ev[i][0].record()
+        g_batched.replay()
+        batched_ev[i][1].record()
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -461,6 +619,7 @@ def main():
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in steps_ev]
     ms = reduce_max(sum(step_ms) / len(step_ms), dev)
+    batched_us = statistics.mean(a.elapsed_time(b) for a, b in batched_ev) * 1e3
     d_ms = statistics.mean(pe[0].elapsed_time(pe[1]) for pe in phase_ev)
     r_ms = statistics.mean(pe[1].elapsed_time(pe[2]) for pe in phase_ev)
     c_ms = statistics.mean(pe[2].elapsed_time(pe[3]) for pe in phase_ev)
@@ -522,13 +681,18 @@ def main():
             "peak_gbs": peak, "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": 2 * launches_per_step * args.steps,
-            "gpu_launches_note": "per step: the round-trip graph plus the same exchange phase by phase",
+            "gpu_launches": (3 * launches_per_step - (wl.A - 1 if wl.F > 1 else 0)) * args.steps,
+            "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase, "
+                                 "and the round trip with one batched collect",
+            "collect_all_us": round(batched_us, 2),
+            "collect_all_note": "the same round trip with afd_source_collect_all (one combine "
+                                "launch for every source) in place of one collect per source",
             "wall_s": round(wall, 3),
             "context": ({"pages_4xH100_nvlink_us": ctx,
                          "note": "multi-GPU communication-only figure from the pages; not this workload"}
                         if ctx else None),
             "sweep": sweep,
+            "native_digest": native_digest(),
         }
         print(json.dumps(line))
     if ws > 1:

@@ -30,7 +30,8 @@ COMBINE_FUSED, COMBINE_TWO_STAGE, COMBINE_TWO_STAGE_FP8 = 0, 1, 2
 
 EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispatch_cached",
            "afd_worker_receive",
-           "afd_worker_reply", "afd_source_collect", "afd_get_error", "afd_clear_error",
+           "afd_worker_reply", "afd_source_collect", "afd_source_collect_all", "afd_get_error",
+           "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
            "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc")
 
@@ -82,6 +83,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_worker_receive": (i32, [v, i32, i32, i32, v, P(Recv)]),
         "afd_worker_reply": (i32, [v, i32, v, i64, u64, v]),
         "afd_source_collect": (i32, [v, i32, v, i32, v, P(View)]),
+        "afd_source_collect_all": (i32, [v, v, i32, v, v]),
         "afd_get_error": (i32, [v, P(i32), P(i32), P(i32), P(i32)]),
         "afd_clear_error": (i32, [v, v]),
         "afd_reset_exchange": (i32, [v]),
@@ -299,6 +301,33 @@ class Buffer:
             base = _wrap(v.data, (T, int(v.row_stride)), torch.bfloat16, self._ctx, self.device)
             return base[:, : self.H]
         return out
+
+    def source_collect_all(self, *, view: bool = False, outs=None, num_tokens=None, stream=None):
+        """Every source's result with one call (one combine launch when F > 1).
+        Returns a list of BF16 [T_s, H] tensors (views with view=True and F == 1)."""
+        if outs is None:
+            if view and self.F == 1:
+                outs = [None] * self.A
+            else:
+                if num_tokens is None:
+                    raise AfdError(ERR_ARG, "pass outs= or num_tokens=")
+                outs = [torch.empty((t, self.H), dtype=torch.bfloat16, device=self.device)
+                        for t in num_tokens]
+        ptrs = (ctypes.c_void_p * self.A)(*[_ptr(o) if o is not None else None for o in outs])
+        views = (View * self.A)()
+        st = self._lib.afd_source_collect_all(self._h, ptrs, int(bool(view)),
+                                              _stream_handle(stream, self.device), views)
+        self._check(st, "source_collect_all")
+        res = []
+        for s in range(self.A):
+            v = views[s]
+            if v.is_view:
+                T = int(v.num_tokens)
+                res.append(_wrap(v.data, (T, int(v.row_stride)), torch.bfloat16, self._ctx,
+                                 self.device)[:, : self.H])
+            else:
+                res.append(outs[s])
+        return res
 
     # -- errors and lifetime ---------------------------------------------------
     def get_error(self):

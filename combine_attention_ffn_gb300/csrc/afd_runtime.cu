@@ -692,6 +692,66 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
   return mark_stream(c, stream);
 }
 
+afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, afd_stream stream_,
+                                  afd_view* views) {
+  if (!c) return AFD_ERR_ARG;
+  const afd_config& g = c->cfg;
+  if (c->phase != kReplied) return fail(c, AFD_ERR_STATE, "replies are not complete");
+  if (c->collected_n != 0) return fail(c, AFD_ERR_STATE, "some sources are already collected");
+  if (!outs && !(view && g.num_workers == 1)) return fail(c, AFD_ERR_ARG, "outs is required");
+  if (g.num_workers == 1) {
+    // copies or views, source by source (no combine runs at collect)
+    for (int s = 0; s < g.num_sources; ++s) {
+      const bool as_view = view && g.num_workers == 1;
+      if (!as_view && c->src[s].T > 0 && (!outs[s] || !aligned16(outs[s])))
+        return fail(c, AFD_ERR_ARG, "outs[%d] must be a 16-byte aligned device pointer", s);
+    }
+    for (int s = 0; s < g.num_sources; ++s) {
+      afd_status st = afd_source_collect(c, s, outs ? outs[s] : nullptr, view, stream_,
+                                         views ? views + s : nullptr);
+      if (st != AFD_OK) return st;
+    }
+    return AFD_OK;
+  }
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  for (int s = 0; s < g.num_sources; ++s)
+    if (c->src[s].T > 0 && (!outs[s] || !aligned16(outs[s])))
+      return fail(c, AFD_ERR_ARG, "outs[%d] must be a 16-byte aligned device pointer", s);
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return fail(c, AFD_ERR_CUDA, "cannot select device %d", c->device);
+  afd_status st = order_stream(c, stream);
+  if (st != AFD_OK) return st;
+  CombineParams p;
+  memset(&p, 0, sizeof p);
+  int tok = 0;
+  for (int s = 0; s < g.num_sources; ++s) {
+    p.routes[s] = c->routes + (int64_t)c->src[s].tok_off * g.top_k;
+    p.out[s] = static_cast<uint16_t*>(outs[s]);
+    p.out_stride[s] = g.hidden;
+    p.tok_off[s] = tok;
+    tok += c->src[s].T;
+  }
+  for (int f = 0; f < g.num_workers; ++f) p.reply[f] = c->reply[f];
+  p.mode = g.combine_mode;
+  p.A = g.num_sources;
+  p.K = g.top_k;
+  p.H = g.hidden;
+  p.total_tokens = tok;
+  cudaError_t e = afd::launch_combine(p, c->sm_cap, stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+  for (int s = 0; s < g.num_sources; ++s) {
+    if (views) {
+      views[s].data = outs[s];
+      views[s].row_stride = g.hidden;
+      views[s].num_tokens = c->src[s].T;
+      views[s].is_view = 0;
+    }
+  }
+  reset_exchange(c);
+  c->gen += 1;
+  return mark_stream(c, stream);
+}
+
 afd_status afd_get_error(afd_ctx* c, int32_t* code, int32_t* source, int32_t* token, int32_t* k) {
   if (!c) return AFD_ERR_ARG;
   if (c->has_last && is_capturing(c->last_stream))

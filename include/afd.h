@@ -247,6 +247,18 @@ typedef struct afd_view {
 AFD_API afd_status afd_source_collect(afd_ctx* ctx, int32_t source, void* out, int32_t view,
                               afd_stream stream, afd_view* view_out);
 
+/* Every source's result at once: for each source s the same as
+ * afd_source_collect(s, outs[s], view, ...), with one combine launch for all
+ * sources when F > 1 (on one GPU the sources' combines are independent, so
+ * they can share a launch). Every source must still be uncollected.
+ *   outs   host array of A device pointers, BF16 [T_s, H] each; an entry may
+ *          be NULL for a source with T = 0, or when view = 1 and F == 1
+ *   view   as in afd_source_collect
+ *   views  host array of A afd_view, filled on success; may be NULL
+ * Errors: as afd_source_collect (nothing is enqueued on an error). */
+AFD_API afd_status afd_source_collect_all(afd_ctx* ctx, void* const* outs, int32_t view,
+                                          afd_stream stream, afd_view* views);
+
 /* The sticky route error found on the GPU. Synchronizes the context's device
  * work first. code = AFD_OK, AFD_ERR_ROUTE_RANGE or AFD_ERR_ROUTE_DUP; for an
  * error, (source, token, k) is the invalid route that comes first in

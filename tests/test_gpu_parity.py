@@ -279,3 +279,29 @@ def test_graph_replay_with_changed_routing(name, T):
         del g
     finally:
         buf.close()
+
+
+@pytest.mark.parametrize("name,T", [("2A2F", 2048), ("2A2F", 8), ("skew-1A3F", 512), ("skew-3A1F", 64),
+                                    ("fp8-2A2F", 128)])
+@pytest.mark.parametrize("view", [False, True])
+def test_collect_all_matches_per_source_collect(name, T, view):
+    """One collect call for every source (one combine launch when F > 1)."""
+    wl = W.named(name, T=T)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE)
+    buf = GH.make_buffer(wl)
+    try:
+        dev = GH.to_device(inp)
+        for s in range(wl.A):
+            buf.source_dispatch(s, dev.x[s], dev.ids[s], dev.w[s], dev.scales[s], bucket=wl.bucket)
+        recvs = {f: buf.worker_receive(f, bucket=wl.bucket) for f in range(wl.F)}
+        reps = {f: GH.expert_reply(wl, f, recvs[f], GH.SCALE) for f in range(wl.F)}
+        for f in range(wl.F):
+            buf.worker_reply(f, reps[f], recvs[f].receipt)
+        res = buf.source_collect_all(view=view, num_tokens=list(wl.T))
+        torch.cuda.synchronize()
+        GH.check_outputs(wl, res, exp)
+        # the exchange is complete: the next one starts normally
+        GH.run_exchange(buf, wl, dev)
+    finally:
+        buf.close()
