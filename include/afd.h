@@ -84,9 +84,10 @@ enum { AFD_BF16 = 0, AFD_FP8_E4M3 = 1 };
  *   in ascending k, one rounding); the partials are added in FP32 in the
  *   order of each worker's last route and rounded once. Equal to FUSED when
  *   F == 1.
- * TWO_STAGE_FP8: as TWO_STAGE, with each partial carried as E4M3 with one
- *   power-of-two scale 2^e per 128 elements (e the smallest integer >= -117
- *   with amax <= 448 * 2^e), the lossy reply format of section 19.
+ * TWO_STAGE_FP8: as TWO_STAGE, with each partial carried as E4M3 values and
+ *   a shared power-of-two factor 2^e for every block of 128 of them (e the
+ *   smallest integer >= -117 with amax <= 448 * 2^e): the lossy reply format
+ *   of section 19.
  * The two-stage modes need top_k <= 8. */
 enum { AFD_COMBINE_FUSED = 0, AFD_COMBINE_TWO_STAGE = 1, AFD_COMBINE_TWO_STAGE_FP8 = 2 };
 

@@ -70,9 +70,9 @@ static int64_t route_index(const orc_problem* p, int s, int t, int k) {
   return ((int64_t)s * p->bucket + t) * p->K + k;
 }
 
-/* Classifies route (s,t,k). "API contract", Roles and tensors: IDs are
- * unique per token, in [0, num_experts), or -1 to skip; anything else is an
- * invalid route. A duplicate is the second (or later) occurrence of an
+/* Classifies route (s,t,k). "API contract", Roles and tensors: an ID is
+ * either -1 (skip) or an expert number in [0, num_experts), and no expert
+ * repeats within a token; anything else is an invalid route. A duplicate is the second (or later) occurrence of an
  * in-range ID inside one token. Returns 1 (valid), 0 (skip, -1) or
  * -ORC_ROUTE_RANGE / -ORC_ROUTE_DUP. */
 static int classify(const orc_problem* p, const int64_t* ids, int s, int t,

@@ -100,8 +100,8 @@ def test_group_exponent_matches_exact_definition(orc):
 
 
 def test_fp8_partial_error_bound(orc):
-    """design page section 19: per element the error is at most 2^-4 of its
-    128-group's amax."""
+    """design page section 19: an element's error stays within 2^-4 times the
+    largest magnitude of its 128-element group."""
     rng = np.random.default_rng(4)
     groups = (rng.standard_normal((500, 128)) * np.exp2(rng.integers(-20, 20, (500, 1)))).astype(np.float32)
     groups = torch.from_numpy(groups).to(torch.bfloat16).float().numpy()
