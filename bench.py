@@ -77,6 +77,21 @@ def algorithmic_bytes(wl, inp, view: bool = False) -> dict:
                 payload=toks * R_in + valid * R_in + valid * 2 * H + toks * 2 * H)
 
 
+def host_cpu() -> dict:
+    """The host's CPU model and core count, for the CPU-baseline record."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                if model:
+                    break
+    except Exception:
+        pass
+    return {"model": model, "nproc": os.cpu_count()}
+
+
 def native_digest() -> str:
     """Hash of the library's sources and header: names the native code a
     record was measured with."""
@@ -233,7 +248,8 @@ def run_reference(args):
                                   l2="not applicable"),
         "gbs": round(ab["total"] / (value * 1e-6) / 1e9, 2),
         "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle"},
+                         "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle",
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "native_digest": native_digest(),
     }
@@ -620,6 +636,26 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in steps_ev]
     ms = reduce_max(sum(step_ms) / len(step_ms), dev)
     batched_us = statistics.mean(a.elapsed_time(b) for a, b in batched_ev) * 1e3
+
+    # the same round trip replayed back to back (L2 not flushed) and issued
+    # eagerly call by call (L2 flushed), outside the timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(50):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    btb_us = e0.elapsed_time(e1) * 1e3 / 50
+    eager = []
+    for _ in range(10):
+        flush.zero_()
+        e0.record()
+        exchange()
+        e1.record()
+        e1.synchronize()
+        eager.append(e0.elapsed_time(e1) * 1e3)
+    eager_us = statistics.median(eager)
     d_ms = statistics.mean(pe[0].elapsed_time(pe[1]) for pe in phase_ev)
     r_ms = statistics.mean(pe[1].elapsed_time(pe[2]) for pe in phase_ev)
     c_ms = statistics.mean(pe[2].elapsed_time(pe[3]) for pe in phase_ev)
@@ -666,7 +702,8 @@ def main():
         times = cpu_oracle_round_trip_us(wl, inp, args.cpu_seconds)
         cpu = {"value": round(statistics.median(times), 1), "unit": "us", "cores": 1, "kind": "oracle",
                "sample": f"{len(times)} full round trips of the same workload "
-                         f"(validate, layout, dispatch, combine; identity expert), single-threaded C"}
+                         f"(validate, layout, dispatch, combine; identity expert), single-threaded C",
+               "host": host_cpu()}
 
     buf.close()
     if rank == 0:
@@ -684,6 +721,8 @@ def main():
             "gpu_launches": (3 * launches_per_step - (wl.A - 1 if wl.F > 1 else 0)) * args.steps,
             "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase, "
                                  "and the round trip with one batched collect",
+            "back_to_back_us": round(btb_us, 2),
+            "eager_us": round(eager_us, 2),
             "collect_all_us": round(batched_us, 2),
             "collect_all_note": "the same round trip with afd_source_collect_all (one combine "
                                 "launch for every source) in place of one collect per source",

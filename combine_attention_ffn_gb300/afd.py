@@ -187,6 +187,9 @@ class Buffer:
         self._ctx = _Context(self._lib, h)
         self._h = h
 
+    # the dtype the top-k IDs must have ("API contract": buffer.topk_idx_dtype)
+    topk_idx_dtype = torch.int64
+
     # -- helpers ------------------------------------------------------------
     def _check(self, st: int, what: str):
         if st != OK:

@@ -16,7 +16,10 @@ constexpr int kChunkWarps = kChunk / 32;
 constexpr int kWorkerShift = 24;     // receipt route code = (worker << 24) | row
 constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
 constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
-constexpr int kSmallRoutes = 4096;   // exchanges up to this many routes take the one-kernel dispatch
+#ifndef AFD_SMALL_ROUTES
+#define AFD_SMALL_ROUTES 4096         // exchanges up to this many routes take the one-kernel dispatch
+#endif
+constexpr int kSmallRoutes = AFD_SMALL_ROUTES;
 constexpr int kSmallSmemMax = 110 * 1024;
 // Launch-shape constants. They only change speed, never results; a build may
 // override them (-D...) to compare shapes.
