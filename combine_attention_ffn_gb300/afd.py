@@ -1,8 +1,10 @@
 """Thin Python binding of libafd (include/afd.h) over ctypes.
 
-Argument marshalling only: tensors become device pointers and sizes, the
-current PyTorch stream becomes the call's stream, and the library's device
-memory comes back as zero-copy tensors. Every step of the exchange runs in
+Argument marshalling only: tensors become pointers and sizes (CUDA tensors,
+or page-locked CPU tensors, which the library reads and writes in place over
+the host link; it refuses pageable ones), the current PyTorch stream becomes
+the call's stream, and the library's device memory comes back as zero-copy
+tensors. Every step of the exchange runs in
 the library's CUDA kernels; there is no fallback. If ``libafd.so`` has not
 been built, :func:`load_library` raises.
 

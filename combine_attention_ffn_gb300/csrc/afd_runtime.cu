@@ -130,6 +130,44 @@ bool is_capturing(cudaStream_t s) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The address the kernels use for a caller buffer: device memory of the
+// context's device, managed memory, or page-locked host memory (reached over
+// the host link through its mapped device address). Pageable host memory is
+// refused: a kernel cannot dereference it.
+afd_status resolve_ptr(afd_ctx* c, const void* p, const char* what, const void** out) {
+  cudaPointerAttributes a;
+  memset(&a, 0, sizeof a);
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, AFD_ERR_ARG, "%s: not a pointer CUDA knows", what);
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      if (a.device != c->device)
+        return fail(c, AFD_ERR_ARG, "%s is on device %d, the context on device %d", what, a.device, c->device);
+      *out = p;
+      return AFD_OK;
+    case cudaMemoryTypeManaged:
+      *out = p;
+      return AFD_OK;
+    case cudaMemoryTypeHost:
+      if (!a.devicePointer) return fail(c, AFD_ERR_ARG, "%s: pinned host memory not mapped for the device", what);
+      *out = a.devicePointer;
+      return AFD_OK;
+    default:
+      return fail(c, AFD_ERR_ARG, "%s is pageable host memory: pin it or copy it to the device", what);
+  }
+}
+
+template <typename T>
+afd_status resolve(afd_ctx* c, T* p, const char* what, T** out) {
+  const void* r = nullptr;
+  afd_status st = resolve_ptr(c, p, what, &r);
+  *out = static_cast<T*>(const_cast<void*>(r));
+  return st;
+}
+
 // Orders `s` after the context's previous call when the stream changes. A
 // wait never crosses a capture boundary (CUDA forbids a captured stream to
 // depend on work recorded outside its capture, and the reverse is
@@ -432,12 +470,21 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
     return fail(c, AFD_ERR_BUCKET, "num_tokens %d outside [0, bucket %d]", num_tokens, bucket);
   if (c->phase == kStaging && (bucket != c->bucket || read_host_counts != c->rhc))
     return fail(c, AFD_ERR_BUCKET, "every role of one exchange passes the same bucket and read_host_counts");
+  const void* dx = nullptr;
+  const int64_t* dids = nullptr;
+  const float* dw = nullptr;
+  const float* dsc = nullptr;
   if (num_tokens > 0) {
     if (!x || !ids || !weights) return fail(c, AFD_ERR_ARG, "x, ids and weights are required");
-    if (!aligned16(x)) return fail(c, AFD_ERR_ARG, "x must be 16-byte aligned");
     if (g.dtype == AFD_FP8_E4M3 && !x_scale) return fail(c, AFD_ERR_ARG, "FP8 dispatch needs x_scale");
     if (g.dtype == AFD_FP8_E4M3 && (scale_stride_t < 0 || scale_stride_b < 0))
       return fail(c, AFD_ERR_ARG, "scale strides must be non-negative");
+    afd_status r = resolve_ptr(c, x, "x", &dx);
+    if (r == AFD_OK) r = resolve(c, ids, "ids", &dids);
+    if (r == AFD_OK) r = resolve(c, weights, "weights", &dw);
+    if (r == AFD_OK && g.dtype == AFD_FP8_E4M3) r = resolve(c, x_scale, "x_scale", &dsc);
+    if (r != AFD_OK) return r;
+    if (!aligned16(dx)) return fail(c, AFD_ERR_ARG, "x must be 16-byte aligned");
   }
   if (read_host_counts && is_capturing(stream))
     return fail(c, AFD_ERR_CAPTURING, "read_host_counts=1 cannot be captured");
@@ -448,10 +495,10 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
   if (st != AFD_OK) return st;
 
   SourceDesc& d = c->src[source];
-  d.x = static_cast<const uint8_t*>(x);
-  d.ids = ids;
-  d.w = weights;
-  d.scale = g.dtype == AFD_FP8_E4M3 ? x_scale : nullptr;
+  d.x = static_cast<const uint8_t*>(dx);
+  d.ids = dids;
+  d.w = dw;
+  d.scale = dsc;
   d.sst = scale_stride_t;
   d.ssb = scale_stride_b;
   d.T = num_tokens;
@@ -488,12 +535,19 @@ afd_status afd_source_dispatch_cached(afd_ctx* c, int32_t source, const void* x,
     return fail(c, AFD_ERR_ARG, "read_host_counts must be 0 or 1");
   if (c->phase == kStaging && read_host_counts != c->rhc)
     return fail(c, AFD_ERR_BUCKET, "every role of one exchange passes the same read_host_counts");
+  const void* dx = nullptr;
+  const float* dw = nullptr;
+  const float* dsc = nullptr;
   if (num_tokens > 0) {
     if (!x) return fail(c, AFD_ERR_ARG, "x is required");
-    if (!aligned16(x)) return fail(c, AFD_ERR_ARG, "x must be 16-byte aligned");
     if (g.dtype == AFD_FP8_E4M3 && !x_scale) return fail(c, AFD_ERR_ARG, "FP8 dispatch needs x_scale");
     if (g.dtype == AFD_FP8_E4M3 && (scale_stride_t < 0 || scale_stride_b < 0))
       return fail(c, AFD_ERR_ARG, "scale strides must be non-negative");
+    afd_status r = resolve_ptr(c, x, "x", &dx);
+    if (r == AFD_OK && weights) r = resolve(c, weights, "weights", &dw);
+    if (r == AFD_OK && g.dtype == AFD_FP8_E4M3) r = resolve(c, x_scale, "x_scale", &dsc);
+    if (r != AFD_OK) return r;
+    if (!aligned16(dx)) return fail(c, AFD_ERR_ARG, "x must be 16-byte aligned");
   }
   if (read_host_counts && is_capturing(stream))
     return fail(c, AFD_ERR_CAPTURING, "read_host_counts=1 cannot be captured");
@@ -503,10 +557,10 @@ afd_status afd_source_dispatch_cached(afd_ctx* c, int32_t source, const void* x,
   if (st != AFD_OK) return st;
 
   SourceDesc& d = c->src[source];
-  d.x = static_cast<const uint8_t*>(x);
+  d.x = static_cast<const uint8_t*>(dx);
   d.ids = nullptr;
-  d.w = num_tokens > 0 ? weights : nullptr;
-  d.scale = g.dtype == AFD_FP8_E4M3 ? x_scale : nullptr;
+  d.w = dw;
+  d.scale = dsc;
   d.sst = scale_stride_t;
   d.ssb = scale_stride_b;
   d.T = num_tokens;
@@ -591,7 +645,11 @@ afd_status afd_worker_reply(afd_ctx* c, int32_t worker, const void* rows, int64_
     return fail(c, AFD_ERR_RECEIPT, "reply has %lld rows, the receive had %lld", (long long)num_rows,
                 (long long)c->recv_rows[worker]);
   if (num_rows > 0 && !rows) return fail(c, AFD_ERR_ARG, "reply rows are required");
-  if (rows && !aligned16(rows)) return fail(c, AFD_ERR_ARG, "reply rows must be 16-byte aligned");
+  if (rows) {
+    afd_status r = resolve_ptr(c, rows, "reply rows", &rows);
+    if (r != AFD_OK) return r;
+    if (!aligned16(rows)) return fail(c, AFD_ERR_ARG, "reply rows must be 16-byte aligned");
+  }
   DeviceGuard guard(c->device);
   if (!guard.ok) return fail(c, AFD_ERR_CUDA, "cannot select device %d", c->device);
   afd_status st = order_stream(c, stream);
@@ -639,8 +697,11 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
   if (view && !view_out) return fail(c, AFD_ERR_ARG, "view = 1 needs view_out");
   const int T = c->src[source].T;
   const bool as_view = view && g.num_workers == 1;
+  void* user_out = out;
   if (!as_view && T > 0) {
     if (!out) return fail(c, AFD_ERR_ARG, "out is required");
+    afd_status r = resolve(c, out, "out", &out);
+    if (r != AFD_OK) return r;
     if (!aligned16(out)) return fail(c, AFD_ERR_ARG, "out must be 16-byte aligned");
   }
   DeviceGuard guard(c->device);
@@ -678,7 +739,7 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
     if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
   }
   if (view_out) {
-    view_out->data = as_view ? static_cast<const void*>(inbox) : static_cast<const void*>(out);
+    view_out->data = as_view ? static_cast<const void*>(inbox) : static_cast<const void*>(user_out);
     view_out->row_stride = g.hidden;
     view_out->num_tokens = T;
     view_out->is_view = as_view ? 1 : 0;
@@ -703,8 +764,13 @@ afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, a
     // copies or views, source by source (no combine runs at collect)
     for (int s = 0; s < g.num_sources; ++s) {
       const bool as_view = view && g.num_workers == 1;
-      if (!as_view && c->src[s].T > 0 && (!outs[s] || !aligned16(outs[s])))
-        return fail(c, AFD_ERR_ARG, "outs[%d] must be a 16-byte aligned device pointer", s);
+      if (!as_view && c->src[s].T > 0) {
+        void* d = nullptr;
+        if (!outs[s]) return fail(c, AFD_ERR_ARG, "outs[%d] is required", s);
+        afd_status r = resolve(c, outs[s], "outs[s]", &d);
+        if (r != AFD_OK) return r;
+        if (!aligned16(d)) return fail(c, AFD_ERR_ARG, "outs[%d] must be 16-byte aligned", s);
+      }
     }
     for (int s = 0; s < g.num_sources; ++s) {
       afd_status st = afd_source_collect(c, s, outs ? outs[s] : nullptr, view, stream_,
@@ -714,9 +780,14 @@ afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, a
     return AFD_OK;
   }
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  for (int s = 0; s < g.num_sources; ++s)
-    if (c->src[s].T > 0 && (!outs[s] || !aligned16(outs[s])))
-      return fail(c, AFD_ERR_ARG, "outs[%d] must be a 16-byte aligned device pointer", s);
+  void* dout[afd::kMaxSources] = {};
+  for (int s = 0; s < g.num_sources; ++s) {
+    if (c->src[s].T == 0) continue;
+    if (!outs[s]) return fail(c, AFD_ERR_ARG, "outs[%d] is required", s);
+    afd_status r = resolve(c, outs[s], "outs[s]", &dout[s]);
+    if (r != AFD_OK) return r;
+    if (!aligned16(dout[s])) return fail(c, AFD_ERR_ARG, "outs[%d] must be 16-byte aligned", s);
+  }
   DeviceGuard guard(c->device);
   if (!guard.ok) return fail(c, AFD_ERR_CUDA, "cannot select device %d", c->device);
   afd_status st = order_stream(c, stream);
@@ -726,7 +797,7 @@ afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, a
   int tok = 0;
   for (int s = 0; s < g.num_sources; ++s) {
     p.routes[s] = c->routes + (int64_t)c->src[s].tok_off * g.top_k;
-    p.out[s] = static_cast<uint16_t*>(outs[s]);
+    p.out[s] = static_cast<uint16_t*>(dout[s]);
     p.out_stride[s] = g.hidden;
     p.tok_off[s] = tok;
     tok += c->src[s].T;

@@ -24,6 +24,12 @@
  *   - Device pointers are addresses on the context's device; host pointers
  *     are noted as such. Every array is dense row-major unless a stride says
  *     otherwise.
+ *   - Wherever a buffer argument below says "device", the call also takes
+ *     managed memory and page-locked host memory (cudaHostAlloc /
+ *     cudaHostRegister; the kernels then read or write it over the host link
+ *     through its mapped device address, with no copy). Pageable host memory,
+ *     memory of another device and pointers CUDA does not know are refused
+ *     with AFD_ERR_ARG before anything is enqueued.
  *   - `stream` is a cudaStream_t of the context's device (NULL = the legacy
  *     default stream). Work is enqueued, never waited for, unless a call says
  *     it synchronizes. When a call uses a different stream from the previous
