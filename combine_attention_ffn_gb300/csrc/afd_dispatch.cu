@@ -20,11 +20,11 @@
 //  * small exchanges (at most kSmallRoutes routes): one kernel. Every block
 //    counts all routes itself (they are few and sit in L2), scans in shared
 //    memory, then copies its share of the rows. No block waits for another.
-//  * large exchanges: layout_kernel (one block per chunk of 256 tokens; the
-//    last block to finish, found with a completion counter, scans the chunk
-//    counts; nobody waits) then scatter_kernel (a warp per token), launched
-//    as a programmatic dependent: its blocks start early and load their first
-//    source rows while the layout is still running.
+//  * large exchanges: cluster_layout_kernel (one thread-block cluster; the
+//    CTAs share their counts through distributed shared memory and write
+//    every route's final row) then scatter_kernel (a warp per token),
+//    launched as a programmatic dependent: its blocks start early and load
+//    their first source rows while the layout is still running.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,12 +34,6 @@
 
 namespace afd {
 namespace {
-
-__device__ __forceinline__ int source_of_chunk(const DispatchParams& p, int g) {
-  int s = 0;
-  while (s + 1 < p.A && g >= p.src[s + 1].chunk_off) ++s;
-  return s;
-}
 
 __device__ __forceinline__ int source_of_token(const DispatchParams& p, int gt) {
   int s = 0;
@@ -235,125 +229,128 @@ __device__ __forceinline__ bool preload_first(const DispatchParams& p, int gwarp
 
 // ---------------------------------------------------------------- large path
 
-// Sums the chunk counts per expert, scans per worker, and writes each chunk's
-// first row per expert. Runs in the last block of the layout launch; the
-// chunk loop of each expert is split into slices so that loads overlap.
-__device__ void layout_finish(const DispatchParams& p, int32_t* sm) {
-  const int E = p.E, G = p.total_chunks, nthr = blockDim.x;
-  const int P = E <= nthr ? nthr / E : 1;  // slices per expert
-  int32_t* part = sm;                      // [P][E]
-  int32_t* sh_total = part + P * E;        // [E]
-  int32_t* sh_start = sh_total + E;        // [E]
-  const int32_t* cc = p.chunk_counts;
+// The layout is one thread-block cluster of n CTAs (n <= 16). CTA r counts
+// the tokens [r * tpc, (r + 1) * tpc) of the flattened (source, token) order
+// (tpc = ceil(N / n)) in slices of 256, keeping a running count per expert in
+// its shared memory, and gives each valid route its rank among the CTA's
+// routes to the same expert. After a cluster barrier every CTA reads all n
+// count vectors through distributed shared memory, so each one computes the
+// totals, the aligned per-worker scan and the first row of its own run of
+// each expert (start[e] plus the counts of CTAs r' < r) without a
+// global-memory round trip. A route's final row is that base plus its rank;
+// the scatter kernel, spread over every SM, adds them up and writes the
+// receipts. Because the CTAs hold consecutive token ranges and ranks follow
+// token order inside a CTA, rows inside an expert follow (source, token)
+// order.
+constexpr int kLocalRankBits = 21;  // layout code = (expert << 21) | rank in the CTA
 
-  for (int idx = threadIdx.x; idx < P * E; idx += nthr) {
-    const int e = idx % E, sl = idx / E;
-    const int g0 = (int)((int64_t)G * sl / P), g1 = (int)((int64_t)G * (sl + 1) / P);
-    int sum = 0, g = g0;
-    for (; g + 8 <= g1; g += 8) {
-      int v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldcg(cc + (int64_t)(g + j) * E + e);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sum += v[j];
-    }
-    for (; g < g1; ++g) sum += __ldcg(cc + (int64_t)g * E + e);
-    part[sl * E + e] = sum;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += nthr) {
-    int run = 0;
-    for (int sl = 0; sl < P; ++sl) {
-      const int v = part[sl * E + e];
-      part[sl * E + e] = run;
-      run += v;
-    }
-    sh_total[e] = run;
-  }
-  __syncthreads();
-  worker_scan(p, sh_total, sh_start, true);
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < P * E; idx += nthr) {
-    const int e = idx % E, sl = idx / E;
-    const int g0 = (int)((int64_t)G * sl / P), g1 = (int)((int64_t)G * (sl + 1) / P);
-    int run = sh_start[e] + part[sl * E + e], g = g0;
-    for (; g + 8 <= g1; g += 8) {
-      int v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldcg(cc + (int64_t)(g + j) * E + e);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        p.chunk_start[(int64_t)(g + j) * E + e] = run;
-        run += v[j];
-      }
-    }
-    for (; g < g1; ++g) {
-      const int c = __ldcg(cc + (int64_t)g * E + e);
-      p.chunk_start[(int64_t)g * E + e] = run;
-      run += c;
-    }
-  }
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Reads the int32 at the same shared-memory offset as `local` in CTA `rank`
+// of this cluster. Only called between cluster barriers, when the value no
+// longer changes, so the loads may be reordered and overlapped freely.
+__device__ __forceinline__ int32_t ld_cluster(const int32_t* local, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  int32_t v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(ra));
+  return v;
 }
 
-__global__ void __launch_bounds__(kChunk) layout_kernel(const __grid_constant__ DispatchParams p) {
+__device__ __forceinline__ int layout_tpc(const DispatchParams& p) {
+  return (p.total_tokens + p.layout_ctas - 1) / p.layout_ctas;
+}
+
+__global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(16) uint32_t smem[];
-  uint32_t* mask = smem;                                                   // [8][E]
-  uint16_t* wbase = reinterpret_cast<uint16_t*>(smem + kChunkWarps * p.E);  // [8][E]
-  __shared__ int is_last;
+  const int E = p.E, K = p.K, N = p.total_tokens;
+  uint32_t* mask = smem;                                        // [8][E]
+  int32_t* wbase = reinterpret_cast<int32_t*>(mask + kChunkWarps * E);  // [8][E]
+  int32_t* cnt = wbase + kChunkWarps * E;                       // [E] this CTA's counts
+  int32_t* total = cnt + E;                                     // [E]
+  int32_t* start = total + E;                                   // [E]
+  int32_t* before = start + E;                                  // [E] counts of earlier CTAs
   pdl_launch_dependents();
 
-  const int E = p.E, K = p.K;
+  const int n = gridDim.x;
+  const uint32_t r = cluster_rank();
+  const int tpc = layout_tpc(p);
+  const int lo = min(N, (int)r * tpc), hi = min(N, lo + tpc);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = blockIdx.x;
+  const uint32_t lanes_before = (1u << lane) - 1u;
 
-  if (g < p.total_chunks) {
-    const int s = source_of_chunk(p, g);
-    const SourceDesc& src = p.src[s];
-    const int t = (g - src.chunk_off) * kChunk + threadIdx.x;
-    const bool live = t < src.T;
-
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int c0 = lo; c0 < hi; c0 += kChunk) {
     for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
     __syncthreads();
-    const int64_t* ids = src.ids + (int64_t)t * K;
-    const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err) : 0u;
-    __syncthreads();
-
-    // Warp offsets inside the chunk and the chunk's count per expert.
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int run = 0;
-#pragma unroll
-      for (int w = 0; w < kChunkWarps; ++w) {
-        wbase[w * E + e] = (uint16_t)run;
-        run += __popc(mask[w * E + e]);
-      }
-      p.chunk_counts[(int64_t)g * E + e] = run;
+    const int gt = c0 + threadIdx.x;
+    const bool live = gt < hi;
+    const int64_t* ids = nullptr;
+    uint32_t valid = 0u;
+    if (live) {
+      const int s = source_of_token(p, gt);
+      const int t = gt - p.src[s].tok_off;
+      ids = p.src[s].ids + (int64_t)t * K;
+      valid = mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err);
     }
     __syncthreads();
-
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = cnt[e];
+#pragma unroll
+      for (int w = 0; w < kChunkWarps; ++w) {
+        wbase[w * E + e] = run;
+        run += __popc(mask[w * E + e]);
+      }
+      cnt[e] = run;
+    }
+    __syncthreads();
     if (live) {
-      int32_t* rt = p.route_tmp + (int64_t)(src.tok_off + t) * K;
-      const uint32_t lanes_before = (1u << lane) - 1u;
+      int32_t* rt = p.route_tmp + (int64_t)gt * K;
       for (int k = 0; k < K; ++k) {
         int code = -1;
         if ((valid >> k) & 1u) {
           const int e = (int)ids[k];
-          const int rank = wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before);
-          code = (e << kRankBits) | rank;
+          code = (e << kLocalRankBits) | (wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before));
         }
         rt[k] = code;
       }
     }
+    __syncthreads();  // the masks are cleared for the next slice
   }
 
-  // The last block to arrive finishes the layout; nobody waits.
-  __threadfence();
+  // Every CTA's counts are final: read them all through the cluster.
+  cluster_arrive();
+  cluster_wait();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int v[kLayoutMaxCtas];
+#pragma unroll
+    for (int q = 0; q < kLayoutMaxCtas; ++q) v[q] = q < n ? ld_cluster(cnt + e, (uint32_t)q) : 0;
+    int b = 0, all = 0;
+#pragma unroll
+    for (int q = 0; q < kLayoutMaxCtas; ++q) {
+      b += q < (int)r ? v[q] : 0;
+      all += v[q];
+    }
+    before[e] = b;
+    total[e] = all;
+  }
+  // no CTA may leave (and free its shared memory) while others still read it
+  cluster_arrive();
   __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(p.done, 1u) == gridDim.x - 1);
+  worker_scan(p, total, start, r == 0);
   __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  layout_finish(p, reinterpret_cast<int32_t*>(smem));
-  if (threadIdx.x == 0) *p.done = 0u;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) p.cta_base[r * E + e] = start[e] + before[e];
+  cluster_wait();
 }
 
 __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid_constant__ DispatchParams p) {
@@ -362,6 +359,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int K = p.K, E = p.E;
+  const int tpc = layout_tpc(p);
 
   // The source rows and weights are inputs, not layout outputs: start loading
   // this warp's first token while the layout kernel is still running.
@@ -369,14 +367,12 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   float pre_w = 0.0f;
   const bool have_pre = preload_first(p, gwarp, pre, pre_w);
   pdl_wait();  // the layout kernel's outputs
-  const int32_t* chunk_start = p.chunk_start;
 
-  auto row_of = [&](int gt, int s, int t, int& e, int& row) -> bool {
-    const int rt = p.route_tmp[(int64_t)gt * K + lane];
-    if (rt < 0) return false;
-    e = rt >> kRankBits;
-    const int g = p.src[s].chunk_off + t / kChunk;
-    row = chunk_start[g * E + e] + (rt & ((1 << kRankBits) - 1));
+  auto row_of = [&](int gt, int, int, int& e, int& row) -> bool {
+    const int code = __ldcg(p.route_tmp + (int64_t)gt * K + lane);
+    if (code < 0) return false;
+    e = code >> kLocalRankBits;
+    row = __ldcg(p.cta_base + (gt / tpc) * E + e) + (code & ((1 << kLocalRankBits) - 1));
     return true;
   };
   int gt = gwarp;
@@ -612,11 +608,9 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   }
 }
 
-size_t layout_smem(int E) {
-  const size_t count = (size_t)kChunkWarps * E * (sizeof(uint32_t) + sizeof(uint16_t));
-  const size_t finish = (size_t)(kChunk + 2 * E) * sizeof(int32_t);
-  return count > finish ? count : finish;
-}
+size_t layout_smem(int E) { return (size_t)kChunkWarps * E * 8 + (size_t)4 * E * 4; }
+
+int g_layout_max_ctas = 0;  // largest cluster the layout kernel can be launched with
 
 size_t small_smem(int E, int N, int K) {
   const int G = (N + kChunk - 1) / kChunk;
@@ -642,18 +636,51 @@ cudaError_t launch(Kernel kernel, int grid, int block, size_t smem, cudaStream_t
 
 }  // namespace
 
+int layout_ctas_for(int total_tokens, int sm_cap) {
+  int n = (total_tokens + kChunk - 1) / kChunk;
+  if (n > g_layout_max_ctas) n = g_layout_max_ctas;
+  if (n > sm_cap) n = sm_cap;
+  return n < 1 ? 1 : n;
+}
+
 bool dispatch_is_small(const DispatchParams& p) {
   return (int64_t)p.total_tokens * p.K <= kSmallRoutes &&
          small_smem(p.E, p.total_tokens, p.K) <= (size_t)kSmallSmemMax;
 }
 
 cudaError_t configure_dispatch_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(cluster_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)layout_smem(kMaxExperts));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(cluster_layout_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
-  return e;
+  if (e != cudaSuccess) return e;
+  // the largest cluster that fits with the largest shared-memory request
+  for (int n = kLayoutMaxCtas; n >= 1; n /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(kChunk);
+    cfg.dynamicSmemBytes = layout_smem(kMaxExperts);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = n;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, cluster_layout_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // this size is not available: try a smaller one
+      continue;
+    }
+    if (clusters >= 1) {
+      g_layout_max_ctas = n;
+      return cudaSuccess;
+    }
+  }
+  return cudaErrorInvalidConfiguration;
 }
 
 // Launches the exchange's dispatch. The first kernel waits for all earlier
@@ -673,8 +700,21 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
     return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,
                   false, p);
   }
-  const int lgrid = p.total_chunks > 0 ? p.total_chunks : 1;
-  cudaError_t e = launch(layout_kernel, lgrid, kChunk, layout_smem(p.E), stream, false, p);
+  // the layout cluster (its size was chosen with the launch parameters)
+  const int n = p.layout_ctas;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n);
+  cfg.blockDim = dim3(kChunk);
+  cfg.dynamicSmemBytes = layout_smem(p.E);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_layout_kernel, p);
   if (e != cudaSuccess) return e;
   // small blocks, a warp per token, so that blocks spread evenly over the SMs
   constexpr int kWarps = AFD_SCATTER_BLOCK / 32;

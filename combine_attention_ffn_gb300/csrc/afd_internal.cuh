@@ -11,13 +11,14 @@ constexpr int kMaxSources = 64;
 constexpr int kMaxWorkers = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kChunk = 256;          // tokens per layout chunk = threads per layout block
+constexpr int kChunk = 256;          // tokens counted per pass = threads per layout block
 constexpr int kChunkWarps = kChunk / 32;
 constexpr int kWorkerShift = 24;     // receipt route code = (worker << 24) | row
 constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
-constexpr int kRankBits = 8;         // layout route code = (expert << 8) | rank in chunk
+constexpr int kLayoutMaxCtas = 16;   // largest layout cluster
+constexpr int kRankBits = 8;         // one-kernel dispatch code = (expert << 8) | rank in chunk
 #ifndef AFD_SMALL_ROUTES
-#define AFD_SMALL_ROUTES 4096         // exchanges up to this many routes take the one-kernel dispatch
+#define AFD_SMALL_ROUTES 1024         // exchanges up to this many routes take the one-kernel dispatch
 #endif
 constexpr int kSmallRoutes = AFD_SMALL_ROUTES;
 constexpr int kSmallSmemMax = 110 * 1024;
@@ -56,8 +57,6 @@ struct SourceDesc {
   int64_t sst, ssb;
   int32_t T;             // live tokens
   int32_t tok_off;       // first flattened token of this source
-  int32_t chunk_off;     // first layout chunk of this source
-  int32_t pad_;
 };
 
 // Everything the layout and scatter kernels of one exchange read or write.
@@ -67,13 +66,11 @@ struct DispatchParams {
   int32_t row_bytes;     // 2H (BF16) or H (FP8)
   int32_t nscale;        // H / 128 for FP8, else 0
   int32_t total_tokens;  // sum of T
-  int32_t total_chunks;  // sum of ceil(T / kChunk)
+  int32_t layout_ctas;   // CTAs of the layout cluster (large path)
   int64_t R_arena;       // rows per worker arena
   // context scratch
-  int32_t* route_tmp;    // [total_tokens][K]: (expert << 8 | rank in chunk) or -1
-  int32_t* chunk_counts; // [total_chunks][E]
-  int32_t* chunk_start;  // [total_chunks][E]: first row of the chunk's run of expert e
-  unsigned int* done;    // last-block counter (returns to 0 after each launch)
+  int32_t* route_tmp;    // [total_tokens][K]: (expert << 21) | rank among the layout CTA's routes, or -1
+  int32_t* cta_base;     // [kLayoutMaxCtas][E]: first row of each layout CTA's run of expert e
   unsigned long long* err;
   // context outputs
   int32_t* starts;       // [E] aligned start of each expert (worker-local rows)
@@ -105,6 +102,7 @@ struct CopyParams {
 
 // Launchers (return the launch's cudaError_t).
 bool dispatch_is_small(const DispatchParams& p);
+int layout_ctas_for(int total_tokens, int sm_cap);
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);

@@ -42,7 +42,6 @@ struct afd_ctx {
   int row_bytes;
   int nscale;
   int64_t R_arena;
-  int max_chunks;
 
   // device arenas (owned)
   uint8_t* rows;
@@ -54,9 +53,7 @@ struct afd_ctx {
   int32_t* hcounts;
   int2* routes;
   int32_t* route_tmp;
-  int32_t* chunk_counts;
-  int32_t* chunk_start;
-  unsigned int* done;
+  int32_t* cta_base;
   unsigned long long* err;
   uint16_t* inbox;
   // pinned host
@@ -222,9 +219,7 @@ void free_all(afd_ctx* c) {
   cudaFree(c->hcounts);
   cudaFree(c->routes);
   cudaFree(c->route_tmp);
-  cudaFree(c->chunk_counts);
-  cudaFree(c->chunk_start);
-  cudaFree(c->done);
+  cudaFree(c->cta_base);
   cudaFree(c->err);
   cudaFree(c->inbox);
   cudaFreeHost(c->host_counts);
@@ -270,15 +265,12 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   const afd_config& g = c->cfg;
   DispatchParams p;
   memset(&p, 0, sizeof p);
-  int tok = 0, chunks = 0;
+  int tok = 0;
   for (int s = 0; s < g.num_sources; ++s) {
     p.src[s] = c->src[s];
     p.src[s].tok_off = tok;
-    p.src[s].chunk_off = chunks;
     c->src[s].tok_off = tok;
-    c->src[s].chunk_off = chunks;
     tok += c->src[s].T;
-    chunks += (c->src[s].T + afd::kChunk - 1) / afd::kChunk;
   }
   p.A = g.num_sources;
   p.F = g.num_workers;
@@ -290,12 +282,10 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   p.row_bytes = c->row_bytes;
   p.nscale = c->nscale;
   p.total_tokens = tok;
-  p.total_chunks = chunks;
   p.R_arena = c->R_arena;
   p.route_tmp = c->route_tmp;
-  p.chunk_counts = c->chunk_counts;
-  p.chunk_start = c->chunk_start;
-  p.done = c->done;
+  p.cta_base = c->cta_base;
+  p.layout_ctas = afd::layout_ctas_for(tok, c->sm_cap);
   p.err = c->err;
   p.starts = c->starts;
   p.ends = c->ends;
@@ -390,7 +380,6 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
     delete c;
     return AFD_ERR_UNSUPPORTED;
   }
-  c->max_chunks = g.num_sources * ((g.capacity + afd::kChunk - 1) / afd::kChunk);
 
   const int64_t F = g.num_workers, A = g.num_sources, E = g.num_experts, K = g.top_k;
   bool ok = dev_alloc(&c->rows, (size_t)(F * c->R_arena * c->row_bytes)) &&
@@ -400,9 +389,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
             dev_alloc(&c->hcounts, (size_t)E) &&
             dev_alloc(&c->routes, (size_t)(A * g.capacity * K)) &&
             dev_alloc(&c->route_tmp, (size_t)(A * g.capacity * K)) &&
-            dev_alloc(&c->chunk_counts, (size_t)(c->max_chunks * E)) &&
-            dev_alloc(&c->chunk_start, (size_t)(c->max_chunks * E)) &&
-            dev_alloc(&c->done, 1) && dev_alloc(&c->err, 1);
+            dev_alloc(&c->cta_base, (size_t)(afd::kLayoutMaxCtas * E)) && dev_alloc(&c->err, 1);
   if (ok && c->nscale) ok = dev_alloc(&c->row_scales, (size_t)(F * c->R_arena * c->nscale));
   if (ok && F == 1) ok = dev_alloc(&c->inbox, (size_t)(A * g.capacity * g.hidden));
   if (ok) ok = cudaMallocHost(reinterpret_cast<void**>(&c->host_counts), E * sizeof(int32_t)) == cudaSuccess;
@@ -414,7 +401,6 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
     return AFD_ERR_OOM;
   }
   cudaError_t e = cudaEventCreateWithFlags(&c->order_ev, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaMemset(c->done, 0, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(c->err, 0xff, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->row_src, 0xff, (size_t)(F * c->R_arena) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->row_w, 0, (size_t)(F * c->R_arena) * sizeof(float));

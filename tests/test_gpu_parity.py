@@ -99,6 +99,25 @@ def test_sm_cap_gives_identical_results(T, sms):
     _roundtrip_check(W.named("2A2F", T=T), num_sms=sms)
 
 
+LARGE_LAYOUTS = [
+    # several 256-token slices per layout CTA
+    W.Workload("many-slices", A=4, F=2, E=128, K=8, H=256, alpha=128, capacity=4096, bucket=4096,
+               T=(4096, 4000, 3000, 4096), seed=611),
+    # top-k 32: the layout's route codes do not fit shared memory
+    W.Workload("wide-topk", A=2, F=4, E=64, K=32, H=256, alpha=8, capacity=2100, bucket=2100,
+               T=(2100, 2033), seed=612),
+    # ragged sources, one of them empty, three workers, alpha 1
+    W.Workload("ragged-5A3F", A=5, F=3, E=96, K=6, H=512, alpha=1, capacity=2048, bucket=2048,
+               T=(0, 2048, 1, 1500, 777), routing="zipf", drop=0.1, seed=613),
+]
+
+
+@pytest.mark.parametrize("wl", LARGE_LAYOUTS, ids=lambda w: w.name)
+def test_parity_large_layouts(wl):
+    _roundtrip_check(wl, mode=GH.SCALE)
+    _roundtrip_check(wl, mode=GH.SCALE, rhc=True, num_sms=5)
+
+
 def test_crafted_fused_ascending_chain_on_gpu():
     """The element whose BF16 result depends on using a fused, ascending
     FP32 chain (worked out in test_oracle_combine): must come out 0x3F81."""
@@ -172,15 +191,21 @@ def test_edge_cases():
         W.Workload("a=5", A=5, F=2, E=32, K=6, H=1024, alpha=16, capacity=200, bucket=160,
                    T=(160, 0, 77, 1, 159)),
         # the one-warp dispatch takes up to 32 tokens, the one-kernel dispatch up
-        # to 4096 routes; both sides of each switch
+        # to 1024 routes; both sides of each switch
         W.Workload("tiny-max", A=1, F=2, E=64, K=8, H=512, alpha=8, capacity=40, bucket=40, T=(32,)),
         W.Workload("tiny-max+1", A=1, F=2, E=64, K=8, H=512, alpha=8, capacity=40, bucket=40, T=(33,)),
         W.Workload("tiny-3src", A=3, F=3, E=96, K=32, H=256, alpha=128, capacity=16, bucket=16, T=(11, 0, 9)),
         W.Workload("small-max", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
+                   T=(1024,)),
+        W.Workload("small-max+1", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
+                   T=(1025,)),
+        W.Workload("cluster-16x256", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
                    T=(4096,)),
         W.Workload("large-min", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
                    T=(4097,)),
         W.Workload("E1024-small", A=2, F=4, E=1024, K=4, H=256, alpha=8, capacity=600, bucket=600,
+                   T=(128, 100)),
+        W.Workload("E1024-mid", A=2, F=4, E=1024, K=4, H=256, alpha=8, capacity=600, bucket=600,
                    T=(512, 500)),
         W.Workload("E1024-large", A=2, F=4, E=1024, K=4, H=256, alpha=8, capacity=600, bucket=600,
                    T=(600, 600)),
