@@ -3,8 +3,8 @@
 One step is one complete exchange: every source dispatches, every worker
 receives and replies (identity expert: the reply is the received rows, as in
 the pages' communication-only numbers), every source collects. The exchange
-is replayed from one CUDA graph; L2 is flushed (a 256 MB write) before every
-timed step, outside the step's events.
+is replayed from one CUDA graph; L2 is flushed (a 256 MB write, then a 256 MB
+read) before every timed step, outside the step's events.
 
 Prints ONE JSON line. `value` is microseconds per round trip (lower is
 better). With --gpus N > 1 (torchrun), every rank runs an independent replica
@@ -133,6 +133,23 @@ def kernel_traffic(kernel: str, workload: str):
     return None
 
 
+class L2Flush:
+    """Evicts L2 (129 MB) between timed steps, outside the steps' events: a
+    256 MB write, then a 256 MB read, so that the write's dirty lines are
+    written back before the step starts instead of during it. The step then
+    finds none of its inputs in L2."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.acc)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons during the timed region."""
 
@@ -258,7 +275,8 @@ def run_reference(args):
 
 
 def workload_config(wl, execution: str = "one CUDA graph per round trip",
-                    l2: str = "flushed before every timed step (256 MB write, outside the step's events)") -> dict:
+                    l2: str = "flushed before every timed step (256 MB write, then 256 MB read so the "
+                              "write-backs finish first; outside the step's events)") -> dict:
     return {"workload": f"{wl.name}: A={wl.A} sources x T={wl.T[0]} tokens, F={wl.F} workers, "
                         f"E={wl.E}, K={wl.K}, H={wl.H}, {wl.dtype}, alpha={wl.alpha}, "
                         f"bucket={wl.bucket}, {wl.routing} routing",
@@ -391,13 +409,13 @@ def run_all_configs(args):
     libbuild.build()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     peak, peak_kind = load_peaks()
 
     def timed(fn, n=15):
         times = []
         for _ in range(n):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -583,9 +601,9 @@ def main():
         with torch.cuda.graph(gp):
             fn()
         g_phase.append(gp)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         g.replay()
         for gp in g_phase:
             gp.replay()
@@ -614,17 +632,17 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         steps_ev[i][0].record()
         g.replay()
         steps_ev[i][1].record()
-        flush.zero_()
+        flush()
         pe = phase_ev[i]
         pe[0].record()
         for j, gp in enumerate(g_phase):
             gp.replay()
             pe[j + 1].record()
-        flush.zero_()
+        flush()
         batched_ev[i][0].record()
         g_batched.replay()
         batched_ev[i][1].record()
@@ -649,7 +667,7 @@ def main():
     btb_us = e0.elapsed_time(e1) * 1e3 / 50
     eager = []
     for _ in range(10):
-        flush.zero_()
+        flush()
         e0.record()
         exchange()
         e1.record()
@@ -774,7 +792,7 @@ def measure_e2e(torch, buf, wl, inp, dev, steps: int, flush):
     def timed(run):
         times = []
         for _ in range(steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run()
@@ -880,7 +898,7 @@ def measure_sweep(torch, afd, W, config, dev, flush):
                     g.replay()
                 times = []
                 for _ in range(10):
-                    flush.zero_()
+                    flush()
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record()
                     g.replay()

@@ -280,6 +280,11 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
   int32_t* total = cnt + E;                                     // [E]
   int32_t* start = total + E;                                   // [E]
   int32_t* before = start + E;                                  // [E] counts of earlier CTAs
+  // The first kernel of an exchange is a programmatic dependent of whatever
+  // ran before it on the stream: it waits for that work (which may produce
+  // the IDs, weights and rows, or still read the arenas) before touching
+  // memory, and only then lets the scatter launch.
+  pdl_wait();
   pdl_launch_dependents();
 
   const int n = gridDim.x;
@@ -397,6 +402,7 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   uint16_t* wbase = reinterpret_cast<uint16_t*>(sh_total + E);    // [8][E]
   uint16_t* ccnt = wbase + kChunkWarps * E;                // [G][E]
 
+  pdl_wait();  // the work before the exchange (see cluster_layout_kernel)
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long* err = blockIdx.x == 0 ? p.err : nullptr;
@@ -491,6 +497,7 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
 // every route's row, so a warp per token only copies the row (and, when new
 // weights are given, refreshes the weights in both receipts).
 __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) cached_scatter_kernel(const __grid_constant__ DispatchParams p) {
+  pdl_wait();  // the work before the exchange (see cluster_layout_kernel)
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -528,6 +535,7 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   uint32_t* mask = tsm;                                     // [E]
   int32_t* sh_start = reinterpret_cast<int32_t*>(mask + E);  // [E]
   int32_t* sh_end = sh_start + E;                           // [E]
+  pdl_wait();  // the work before the exchange (see cluster_layout_kernel)
   pdl_launch_dependents();
   const int lane = threadIdx.x;
 
@@ -683,22 +691,25 @@ cudaError_t configure_dispatch_kernels() {
   return cudaErrorInvalidConfiguration;
 }
 
-// Launches the exchange's dispatch. The first kernel waits for all earlier
-// work on the stream (a normal launch), so it never overlaps the previous
-// exchange's combine, which still reads the arenas it overwrites.
+// Launches the exchange's dispatch. Every kernel is a programmatic dependent
+// of the one before it. The first one waits (griddepcontrol.wait) for all
+// earlier work on the stream before it reads or writes anything, so it never
+// overlaps the producer of its inputs or the previous exchange's combine,
+// which still reads the arenas; it lets its own dependents launch only after
+// that wait.
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   const int block = 256;
   if (p.total_tokens >= 1 && p.total_tokens <= 32 && AFD_TINY_DISPATCH) {
     // one block per token, and at least 16 blocks to share the padding rows
     const int grid = p.total_tokens > 16 ? p.total_tokens : 16;
-    return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, false, p);
+    return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, true, p);
   }
   if (dispatch_is_small(p)) {
     int grid = (p.total_tokens + 7) / 8;
     if (grid > sm_cap) grid = sm_cap;
     if (grid < 1) grid = 1;
     return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,
-                  false, p);
+                  true, p);
   }
   // the layout cluster (its size was chosen with the launch parameters)
   const int n = p.layout_ctas;
@@ -707,13 +718,15 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
   cfg.blockDim = dim3(kChunk);
   cfg.dynamicSmemBytes = layout_smem(p.E);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = n;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, cluster_layout_kernel, p);
   if (e != cudaSuccess) return e;
   // small blocks, a warp per token, so that blocks spread evenly over the SMs
@@ -728,14 +741,14 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
 
 namespace afd {
 
-// Launched normally (not as a programmatic dependent): it rewrites the rows
-// that the previous exchange's combine reads.
+// A programmatic dependent of the work before it, which it waits for before
+// it rewrites the rows that the previous exchange's combine reads.
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   constexpr int kWarps = AFD_SCATTER_BLOCK / 32;
   int grid = (p.total_tokens + kWarps - 1) / kWarps;
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
-  return launch(cached_scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, false, p);
+  return launch(cached_scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
 }
 
 }  // namespace afd
