@@ -854,9 +854,11 @@ def measure_e2e(torch, buf, wl, inp, dev, steps: int, flush):
 
 
 def measure_sweep(torch, afd, W, config, dev, flush):
-    """Graph-replayed round trip at the workload's other token counts
-    (L2 flushed before each replay), with a full dispatch and with a cached
-    dispatch (the last exchange's routing reused)."""
+    """Graph-replayed round trip at the workload's other token counts, with a
+    full dispatch, with a cached dispatch (the last exchange's routing
+    reused), and with a full dispatch and one batched collect. Each is timed
+    with L2 flushed before every replay, and replayed 50 times back to back
+    (small batches then stay in L2, as they would between decode steps)."""
     out = {}
     table = {"2A2F": (1, 8, 32, 128, 512, 2048), "2A2F-H4096": (1, 128, 2048)}
     for name, Ts in (("2A2F", table["2A2F"]), ("2A2F-H4096", table["2A2F-H4096"])):
@@ -888,7 +890,16 @@ def measure_sweep(torch, afd, W, config, dev, flush):
                 for s in range(wl.A):
                     buf.source_collect(s, out=outs[s])
 
-            for label, fn in (("", exchange), (" cached", exchange_cached)):
+            def exchange_batched():
+                for s in range(wl.A):
+                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
+                for f in range(wl.F):
+                    r = buf.worker_receive(f, bucket=wl.bucket)
+                    buf.worker_reply(f, r.rows, r.receipt)
+                buf.source_collect_all(outs=outs)
+
+            for label, fn in (("", exchange), (" cached", exchange_cached),
+                              (" batched collect", exchange_batched)):
                 fn()
                 torch.cuda.synchronize()
                 g = torch.cuda.CUDAGraph()
@@ -905,8 +916,15 @@ def measure_sweep(torch, afd, W, config, dev, flush):
                     b.record()
                     b.synchronize()
                     times.append(a.elapsed_time(b) * 1e3)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(50):
+                    g.replay()
+                b.record()
+                b.synchronize()
                 del g
                 out[f"{name} T={T}{label}"] = round(statistics.median(times), 2)
+                out[f"{name} T={T}{label} back to back"] = round(a.elapsed_time(b) * 1e3 / 50, 2)
             buf.close()
     return out
 
