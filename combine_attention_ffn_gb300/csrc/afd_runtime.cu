@@ -132,6 +132,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the host link through its mapped device address). Pageable host memory is
 // refused: a kernel cannot dereference it.
 afd_status resolve_ptr(afd_ctx* c, const void* p, const char* what, const void** out) {
+  DeviceGuard guard(c->device);  // a mapped host address is the current device's
   cudaPointerAttributes a;
   memset(&a, 0, sizeof a);
   cudaError_t e = cudaPointerGetAttributes(&a, p);
