@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "afd.h"
 #include "afd_device.cuh"
 #include "afd_internal.cuh"
 
@@ -113,80 +114,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   }
 }
 
-// Large batches, K <= 8: a warp per token. The token's route codes are read
-// once; the hidden row is then walked in 512-byte segments (one 16-byte
-// slice per lane) with a two-stage register pipeline: the loads of segment
-// i+1 (one per route) are in flight while segment i is summed and stored.
-__device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* const (&rowp)[kGroup],
-                                         uint32_t okmask, int v) {
-#pragma unroll
-  for (int j = 0; j < kGroup; ++j)
-    if ((okmask >> j) & 1u) buf[j] = ld_once(reinterpret_cast<const uint4*>(rowp[j]) + v);
-}
-
-__device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGroup],
-                                        const float (&wk)[kGroup], uint32_t okmask, int v) {
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-#pragma unroll
-  for (int j = 0; j < kGroup; ++j)
-    if ((okmask >> j) & 1u) fma8(acc, wk[j], buf[j]);
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  out_row[v] = o;
-}
-
-__global__ void __launch_bounds__(64) combine_token_kernel(const __grid_constant__ CombineParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K;
-  // a warp takes 1/split of a token's segments (split divides the count)
-  const int nseg_all = p.H >> 8;
-  const int split = nseg_all % AFD_COMBINE_SPLIT == 0 ? AFD_COMBINE_SPLIT : 1;
-  const int nseg = nseg_all / split;
-  const int items = p.total_tokens * split;
-
-  for (int item = gwarp; item < items; item += nwarps) {
-    const int gt = item / split;
-    const int seg0 = (item - gt * split) * nseg;
-    const int s = source_of(p, gt);
-    const int t = gt - p.tok_off[s];
-    int2 r = make_int2(-1, 0);
-    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
-    const uint16_t* rowp[kGroup];
-    float wk[kGroup];
-    uint32_t okmask = 0u;
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      const int c = __shfl_sync(0xffffffffu, r.x, j);
-      wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
-      const bool ok = (j < K) && (c >= 0);
-      okmask |= (ok ? 1u : 0u) << j;
-      rowp[j] = ok ? p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
-    }
-    uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]) + seg0 * 32;
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
-    uint4 a[kGroup], b[kGroup];
-    load_seg(a, rowp, okmask, lane);
-    int seg = 0;
-    for (; seg + 2 <= nseg; seg += 2) {
-      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane);
-      sum_seg(out_row, a, wk, okmask, seg * 32 + lane);
-      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane);
-      sum_seg(out_row, b, wk, okmask, (seg + 1) * 32 + lane);
-    }
-    if (seg < nseg) sum_seg(out_row, a, wk, okmask, seg * 32 + lane);
-  }
-}
-
 // ---- two-stage combine (optionally with E4M3 partials) ----
 
 __device__ __forceinline__ float bf16_round(float v) {
@@ -219,41 +146,56 @@ __device__ __forceinline__ void e4m3_round_trip2(float& a, float& b) {
   b = __low2float(hv);
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_constant__ CombineParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int K = p.K;  // <= kGroup
-  const int nseg = p.H >> 8;
-  const int64_t items = (int64_t)p.total_tokens * nseg;
+// ---- per-token combine ----
 
-  for (int64_t it = gwarp; it < items; it += nwarps) {
-    const int gt = (int)(it / nseg);
-    const int seg = (int)(it - (int64_t)gt * nseg);
-    const int s = source_of(p, gt);
-    const int t = gt - p.tok_off[s];
-    int2 r = make_int2(-1, 0);
-    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
-    const int v = seg * 32 + lane;
-
-    uint4 buf[kGroup];
-    float wk[kGroup];
-    int wf[kGroup];  // worker of each valid route, -1 otherwise
+// Large batches, K <= 8: a warp per token. The token's route codes are read
+// once; the hidden row is then walked in 512-byte segments (one 16-byte
+// slice per lane) with a two-stage register pipeline: the loads of segment
+// i+1 (one per route) are in flight while segment i is summed and stored.
+//
+// The token's routes from its receipt entries (lane j < K holds route j):
+// row pointers, weights and workers (-1 for a skipped route). Returns the
+// valid routes as bits.
+__device__ __forceinline__ uint32_t token_routes(const CombineParams& p, int2 r, const uint16_t* (&rowp)[kGroup],
+                                                 float (&wk)[kGroup], int (&wf)[kGroup]) {
+  uint32_t okmask = 0u;
 #pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      const int c = __shfl_sync(0xffffffffu, r.x, j);
-      wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
-      wf[j] = (j < K && c >= 0) ? (c >> kWorkerShift) : -1;
-      if (wf[j] >= 0)
-        buf[j] = ld_once(reinterpret_cast<const uint4*>(p.reply[wf[j]] + (int64_t)(c & kRowMask) * p.H) + v);
-    }
+  for (int j = 0; j < kGroup; ++j) {
+    const int c = __shfl_sync(0xffffffffu, r.x, j);
+    wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
+    const bool ok = (j < p.K) && (c >= 0);
+    okmask |= (ok ? 1u : 0u) << j;
+    wf[j] = ok ? (c >> kWorkerShift) : -1;
+    rowp[j] = ok ? p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
+  }
+  return okmask;
+}
 
-    float acc[8];
+__device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* const (&rowp)[kGroup],
+                                         uint32_t okmask, int v) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  for (int j = 0; j < kGroup; ++j)
+    if ((okmask >> j) & 1u) buf[j] = ld_once(reinterpret_cast<const uint4*>(rowp[j]) + v);
+}
+
+// Sums one segment (this lane's 8 elements of every route) and stores it.
+// AFD_COMBINE_FUSED: one FP32 chain over the routes in ascending k, one BF16
+// rounding. Two-stage modes (design page, section 19): each worker's routes
+// form a partial (FP32 chain in ascending k, rounded to BF16; in the FP8
+// mode also scaled by its group's power of two, rounded to E4M3 and back);
+// the partials are added in FP32 in the order of each worker's last route,
+// then rounded to BF16 once.
+template <int kMode>
+__device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGroup], const float (&wk)[kGroup],
+                                        const int (&wf)[kGroup], uint32_t okmask, int v) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  if (kMode == AFD_COMBINE_FUSED) {
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j)
+      if ((okmask >> j) & 1u) fma8(acc, wk[j], buf[j]);
+  } else {
 #pragma unroll
     for (int k = 0; k < kGroup; ++k) {
       if (wf[k] < 0) continue;
@@ -261,7 +203,6 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
 #pragma unroll
       for (int j = k + 1; j < kGroup; ++j) last = last && (wf[j] != wf[k]);
       if (!last) continue;
-      // this worker's partial: its routes in ascending k, one BF16 rounding
       float part[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) part[e] = 0.0f;
@@ -270,7 +211,7 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
         if (wf[j] == wf[k]) fma8(part, wk[j], buf[j]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) part[e] = bf16_round(part[e]);
-      if (kFp8) {
+      if (kMode == AFD_COMBINE_TWO_STAGE_FP8) {
         // one power-of-two scale per 128 elements: 16 lanes x 8 elements
         float amax = 0.0f;
 #pragma unroll
@@ -290,12 +231,84 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = acc[e] + part[e];
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s])[v] = o;
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  out_row[v] = o;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_STAGE_BLOCKS) combine_token_kernel(const __grid_constant__ CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;
+  // a warp takes 1/split of a token's segments (split divides the count)
+  const int nseg_all = p.H >> 8;
+  const int split = nseg_all % AFD_COMBINE_SPLIT == 0 ? AFD_COMBINE_SPLIT : 1;
+  const int nseg = nseg_all / split;
+  const int items = p.total_tokens * split;
+
+  for (int item = gwarp; item < items; item += nwarps) {
+    const int gt = item / split;
+    const int seg0 = (item - gt * split) * nseg;
+    const int s = source_of(p, gt);
+    const int t = gt - p.tok_off[s];
+    int2 r = make_int2(-1, 0);
+    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    const uint16_t* rowp[kGroup];
+    float wk[kGroup];
+    int wf[kGroup];
+    const uint32_t okmask = token_routes(p, r, rowp, wk, wf);
+    uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]) + seg0 * 32;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
+    uint4 a[kGroup], b[kGroup];
+    load_seg(a, rowp, okmask, lane);
+    int seg = 0;
+    for (; seg + 2 <= nseg; seg += 2) {
+      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane);
+      sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
+      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane);
+      sum_seg<kMode>(out_row, b, wk, wf, okmask, (seg + 1) * 32 + lane);
+    }
+    if (seg < nseg) sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
+  }
+}
+
+// Few tokens: a warp per (token, 512-byte segment), as combine_kernel<1>,
+// with the two-stage rule.
+template <int kMode>
+__global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_constant__ CombineParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;  // <= kGroup
+  const int nseg = p.H >> 8;
+  const int64_t items = (int64_t)p.total_tokens * nseg;
+
+  for (int64_t it = gwarp; it < items; it += nwarps) {
+    const int gt = (int)(it / nseg);
+    const int seg = (int)(it - (int64_t)gt * nseg);
+    const int s = source_of(p, gt);
+    const int t = gt - p.tok_off[s];
+    int2 r = make_int2(-1, 0);
+    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    const uint16_t* rowp[kGroup];
+    float wk[kGroup];
+    int wf[kGroup];
+    const uint32_t okmask = token_routes(p, r, rowp, wk, wf);
+    uint4 buf[kGroup];
+    load_seg(buf, rowp, okmask, seg * 32 + lane);
+    sum_seg<kMode>(reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]), buf, wk, wf,
+                   okmask, seg * 32 + lane);
   }
 }
 
@@ -334,19 +347,25 @@ cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stre
 // stream and wait for it before reading anything.
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
   if (p.total_tokens <= 0) return cudaSuccess;
-  if (p.mode != 0) {
-    const int64_t items = (int64_t)p.total_tokens * (p.H >> 8);
-    int64_t grid = (items + 7) / 8;
-    if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
-    return p.mode == 2 ? launch_pdl(combine_two_stage_kernel<true>, grid, 256, stream, p)
-                       : launch_pdl(combine_two_stage_kernel<false>, grid, 256, stream, p);
-  }
   if (p.K <= kGroup && p.total_tokens >= sm_cap * AFD_TOKEN_COMBINE_MIN) {
     // enough tokens for a warp each on every SM: the pipelined per-token
     // kernel, in two-warp blocks so that tokens spread evenly over the SMs
     int64_t grid = ((int64_t)p.total_tokens * AFD_COMBINE_SPLIT + 1) / 2;
     if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
-    return launch_pdl(combine_token_kernel, grid, 64, stream, p);
+    switch (p.mode) {
+      case AFD_COMBINE_TWO_STAGE: return launch_pdl(combine_token_kernel<AFD_COMBINE_TWO_STAGE>, grid, 64, stream, p);
+      case AFD_COMBINE_TWO_STAGE_FP8:
+        return launch_pdl(combine_token_kernel<AFD_COMBINE_TWO_STAGE_FP8>, grid, 64, stream, p);
+      default: return launch_pdl(combine_token_kernel<AFD_COMBINE_FUSED>, grid, 64, stream, p);
+    }
+  }
+  if (p.mode != AFD_COMBINE_FUSED) {
+    const int64_t items = (int64_t)p.total_tokens * (p.H >> 8);
+    int64_t grid = (items + 7) / 8;
+    if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
+    return p.mode == AFD_COMBINE_TWO_STAGE_FP8
+               ? launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>, grid, 256, stream, p)
+               : launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>, grid, 256, stream, p);
   }
   const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
   const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps

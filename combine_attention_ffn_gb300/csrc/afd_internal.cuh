@@ -33,6 +33,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_COMBINE_SPLIT
 #define AFD_COMBINE_SPLIT 1       // warps per token in the per-token combine
 #endif
+#ifndef AFD_TWO_STAGE_BLOCKS
+#define AFD_TWO_STAGE_BLOCKS 7    // resident two-warp blocks per SM asked of the two-stage per-token combine
+#endif
 #ifndef AFD_TOKEN_COMBINE_MIN
 #define AFD_TOKEN_COMBINE_MIN 8  // x SMs: tokens from which the per-token combine is used
 #endif

@@ -29,7 +29,10 @@ MODES = [afd.COMBINE_TWO_STAGE, afd.COMBINE_TWO_STAGE_FP8]
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name,T", [("tiny", None), ("2A2F", 1), ("2A2F", 128), ("2A2F", 2048),
                                     ("2A2F-H4096", 128), ("skew-1A3F", 512), ("skew-3A1F", 64),
-                                    ("fp8-2A2F", 128)])
+                                    ("fp8-2A2F", 128),
+                                    # per-token kernels (at least 8 tokens per SM)
+                                    ("2A2F-H4096", 2048), ("skew-1A3F", 2048), ("skew-3A1F", 2048),
+                                    ("fp8-2A2F", 2048)])
 def test_two_stage_matches_oracle(mode, name, T):
     wl = W.named(name, T=T)
     inp = W.make_inputs(wl)
