@@ -10,6 +10,7 @@ import json
 import os
 import shutil
 import subprocess
+import sys
 from fractions import Fraction
 
 import numpy as np
@@ -61,11 +62,22 @@ MUTATIONS = {
     "worker_order_first_route": ("for (int j = k + 1; j < p->K; ++j) {\n          int64_t rj = route_index(p, s, t, j);\n          if (slot[rj] >= 0 && (int)(ids[rj] / Ef) == f) last = 0;",
                                  "for (int j = 0; j < k; ++j) {\n          int64_t rj = route_index(p, s, t, j);\n          if (slot[rj] >= 0 && (int)(ids[rj] / Ef) == f) last = 0;"),
     "fp8_dequant_wrong_scale": ("part[h] = ldexpf(orc_e4m3_to_float(q), e);", "part[h] = ldexpf(orc_e4m3_to_float(q), e + 1);"),
+    "dispatch_worker_modulo": ("int f = (int)(e / Ef);", "int f = (int)(e % p->F);"),
+    "combine_worker_modulo": ("int f = (int)(ids[ri] / Ef);\n          float r",
+                              "int f = (int)(ids[ri] % p->F);\n          float r"),
+    "ends_without_count": ("ends[i] = start[i] + count[i];", "ends[i] = start[i];"),
+    "padding_weight_one": ("row_w[f * r_stride + r] = 0.0f;", "row_w[f * r_stride + r] = 1.0f;"),
+    "combine_weight_squared": ("acc = fmaf(w[ri], r, acc);", "acc = fmaf(w[ri] * w[ri], r, acc);"),
+    "fp8_scale_from_first_block": ("x_scales[((int64_t)s * p->bucket + t) * nb + b];",
+                                   "x_scales[((int64_t)s * p->bucket + t) * nb];"),
+    "expert_skips_last_row": ("for (int64_t r = start[e]; r < ends[e]; ++r) {",
+                              "for (int64_t r = start[e]; r < ends[e] - 1; ++r) {"),
 }
 
 
-def _pins(orc) -> list:
-    """Runs the battery; returns the names of the pins that failed."""
+def _pins(orc, report=None) -> list:
+    """Runs the battery; returns the names of the pins that failed. `report`,
+    when given, is called with each failed pin's name as soon as it fails."""
     failed = []
 
     def run(name, fn):
@@ -73,6 +85,8 @@ def _pins(orc) -> list:
             fn()
         except Exception:  # a wrong value, or results too broken to index
             failed.append(name)
+            if report:
+                report(name)
 
     def golden_layout():
         with open(os.path.join(GOLDEN, "ends_convention.json")) as fh:
@@ -81,6 +95,9 @@ def _pins(orc) -> list:
         p = oracle.Problem(q["A"], q["F"], q["E"], q["K"], q["H"], q["alpha"], q["bucket"],
                            oracle.BF16, q["T"])
         ids = np.array(g["ids"], np.int64)
+        lay = oracle.layout(p, ids, orc)  # the layout alone first: no arrays sized by it yet
+        for key in ("count", "start", "ends", "host_counts", "r_exact"):
+            assert np.array_equal(np.asarray(lay[key]), np.array(g[key])), key
         r = oracle.round_trip(p, ids, np.ones(ids.shape, np.float32),
                               np.zeros((1, q["bucket"], q["H"]), np.uint16), orc=orc)
         for key in ("count", "start", "ends", "host_counts", "r_exact", "slot"):
@@ -215,7 +232,7 @@ def _pins(orc) -> list:
     return failed
 
 
-def _build_variant(tmp_path, name, old, new):
+def _build_variant(tmp_path, name, old, new) -> str:
     src = open(SRC).read()
     assert src.count(old) == 1, f"{name}: pattern must occur once"
     d = tmp_path / name
@@ -225,7 +242,24 @@ def _build_variant(tmp_path, name, old, new):
     lib = d / "liborc.so"
     subprocess.run(["gcc", *oracle.CFLAGS, "-I", str(d), str(d / "orc.c"), "-o", str(lib), "-lm"],
                    check=True)
-    return oracle.Oracle(str(lib))
+    return str(lib)
+
+
+def _pins_in_child(lib: str):
+    """Runs the battery on a mutant library in a child process, so that a
+    mutant that writes out of bounds cannot take the test run down with it.
+    Returns the pins that failed before the end or a crash, and "(crashed)"
+    when the child did not finish."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import sys; sys.path[:0] = [%r, %r]; import oracle, test_oracle_mutations as M; "
+            "M._pins(oracle.Oracle(%r), report=lambda n: print('FAILED ' + n, flush=True)); "
+            "print('DONE', flush=True)" % (here, os.path.dirname(here), lib))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    lines = r.stdout.splitlines()
+    failed = [l[7:] for l in lines if l.startswith("FAILED ")]
+    if r.returncode != 0 or "DONE" not in lines:
+        failed.append("(crashed)")
+    return failed
 
 
 def test_unmodified_oracle_passes_battery(orc):
@@ -235,6 +269,5 @@ def test_unmodified_oracle_passes_battery(orc):
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_is_caught(tmp_path, name):
     old, new = MUTATIONS[name]
-    mutant = _build_variant(tmp_path, name, old, new)
-    failed = _pins(mutant)
-    assert failed, f"mistake '{name}' passed every pin"
+    failed = _pins_in_child(_build_variant(tmp_path, name, old, new))
+    assert [f for f in failed if f != "(crashed)"], f"mistake '{name}' passed every pin ({failed})"
