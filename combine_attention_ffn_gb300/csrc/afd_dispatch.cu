@@ -618,7 +618,6 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
 
 size_t layout_smem(int E) { return (size_t)kChunkWarps * E * 8 + (size_t)4 * E * 4; }
 
-int g_layout_max_ctas = 0;  // largest cluster the layout kernel can be launched with
 
 size_t small_smem(int E, int N, int K) {
   const int G = (N + kChunk - 1) / kChunk;
@@ -644,9 +643,9 @@ cudaError_t launch(Kernel kernel, int grid, int block, size_t smem, cudaStream_t
 
 }  // namespace
 
-int layout_ctas_for(int total_tokens, int sm_cap) {
+int layout_ctas_for(int total_tokens, int sm_cap, int max_ctas) {
   int n = (total_tokens + kChunk - 1) / kChunk;
-  if (n > g_layout_max_ctas) n = g_layout_max_ctas;
+  if (n > max_ctas) n = max_ctas;
   if (n > sm_cap) n = sm_cap;
   return n < 1 ? 1 : n;
 }
@@ -656,7 +655,9 @@ bool dispatch_is_small(const DispatchParams& p) {
          small_smem(p.E, p.total_tokens, p.K) <= (size_t)kSmallSmemMax;
 }
 
-cudaError_t configure_dispatch_kernels() {
+// Sets the kernels' shared-memory and cluster attributes on the current
+// device and returns in *max_ctas the largest layout cluster it can run.
+cudaError_t configure_dispatch_kernels(int* max_ctas) {
   cudaError_t e = cudaFuncSetAttribute(cluster_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)layout_smem(kMaxExperts));
   if (e == cudaSuccess)
@@ -684,7 +685,7 @@ cudaError_t configure_dispatch_kernels() {
       continue;
     }
     if (clusters >= 1) {
-      g_layout_max_ctas = n;
+      *max_ctas = n;
       return cudaSuccess;
     }
   }

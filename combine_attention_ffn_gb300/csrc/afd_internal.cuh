@@ -105,11 +105,11 @@ struct CopyParams {
 
 // Launchers (return the launch's cudaError_t).
 bool dispatch_is_small(const DispatchParams& p);
-int layout_ctas_for(int total_tokens, int sm_cap);
+int layout_ctas_for(int total_tokens, int sm_cap, int max_ctas);
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
-cudaError_t configure_dispatch_kernels();
+cudaError_t configure_dispatch_kernels(int* max_ctas);
 
 }  // namespace afd

@@ -38,6 +38,7 @@ struct afd_ctx {
   int device;
   int sm_count;
   int sm_cap;
+  int layout_max_ctas;  // largest layout cluster this device runs
   int Ef;
   int row_bytes;
   int nscale;
@@ -286,7 +287,7 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   p.R_arena = c->R_arena;
   p.route_tmp = c->route_tmp;
   p.cta_base = c->cta_base;
-  p.layout_ctas = afd::layout_ctas_for(tok, c->sm_cap);
+  p.layout_ctas = afd::layout_ctas_for(tok, c->sm_cap, c->layout_max_ctas);
   p.err = c->err;
   p.starts = c->starts;
   p.ends = c->ends;
@@ -405,7 +406,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->err, 0xff, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->row_src, 0xff, (size_t)(F * c->R_arena) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->row_w, 0, (size_t)(F * c->R_arena) * sizeof(float));
-  if (e == cudaSuccess) e = afd::configure_dispatch_kernels();
+  if (e == cudaSuccess) e = afd::configure_dispatch_kernels(&c->layout_max_ctas);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     fprintf(stderr, "afd_create: %s\n", cudaGetErrorString(e));
