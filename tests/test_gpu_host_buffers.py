@@ -143,3 +143,32 @@ def test_pinned_host_buffers_in_a_captured_graph():
         del g
     finally:
         buf.close()
+
+
+def test_cached_dispatch_from_pinned_host_inputs():
+    """A cached dispatch (the last routing reused) reading new activations and
+    weights straight from pinned host memory matches a full dispatch of the
+    same IDs from device memory."""
+    wl = W.named("2A2F", T=300)
+    inp = W.make_inputs(wl)
+    buf = GH.make_buffer(wl)
+    try:
+        GH.run_exchange(buf, wl, GH.to_device(inp), mode=GH.SCALE)
+        other = W.make_inputs(W.Workload(**{**wl.__dict__, "seed": wl.seed + 5}))
+        w = other.w.copy()
+        w[inp.ids < 0] = inp.w[inp.ids < 0]
+        new = W.Inputs(wl, inp.ids.copy(), w, other.x.copy(), None)
+        exp = GH.expected(new, GH.SCALE)
+        host = _pinned(new)
+        for s in range(wl.A):
+            buf.source_dispatch_cached(s, host.x[s], host.w[s], bucket=wl.bucket)
+        recvs = {f: buf.worker_receive(f, bucket=wl.bucket) for f in range(wl.F)}
+        replies = {f: GH.expert_reply(wl, f, recvs[f], GH.SCALE) for f in range(wl.F)}  # kept alive
+        for f in range(wl.F):
+            buf.worker_reply(f, replies[f], recvs[f].receipt)
+        res = buf.source_collect_all(outs=GH.alloc_outs(wl))
+        torch.cuda.synchronize()
+        GH.check_layout(wl, GH.snapshot(recvs), exp, False, buf)
+        GH.check_outputs(wl, res, exp)
+    finally:
+        buf.close()
