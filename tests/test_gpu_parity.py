@@ -273,7 +273,9 @@ def test_roles_on_separate_streams():
         buf.close()
 
 
-@pytest.mark.parametrize("name,T", [("2A2F", 128), ("fp8-2A1F", 64), ("skew-1A3F", 512)])
+@pytest.mark.parametrize("name,T", [("2A2F", 128), ("fp8-2A1F", 64), ("skew-1A3F", 512),
+                                    # the benchmark's launch configuration
+                                    ("2A2F", 2048), ("2A2F-H4096", 2048)])
 def test_graph_replay_with_changed_routing(name, T):
     """Capture one complete exchange, then change IDs, weights and payloads in
     place and replay; every replay must match the oracle on its new inputs."""
