@@ -524,11 +524,89 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) cached_scatter_kernel(const
 
 // ---------------------------------------------------------------- tiny path
 
-// At most 32 tokens in the whole exchange: one-warp blocks. Every block
+// One warp scans all E experts in one pass: lane i owns the experts
+// [i * epl, (i + 1) * epl), epl = ceil(E / 32); the first expert of every
+// worker starts a new segment of the (segmented) scan of aligned counts.
+// count_of(e) gives expert e's count. Writes sh_start / sh_end, and with
+// `out` the context's starts, ends and aligned counts.
+template <typename CountOf>
+__device__ __forceinline__ void warp_worker_scan(const DispatchParams& p, CountOf count_of,
+                                                 int32_t* sh_start, int32_t* sh_end, bool out) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, Ef = p.Ef;
+  const int epl = (E + 31) >> 5;
+  const int e0 = lane * epl, e1 = min(E, e0 + epl);
+  // the sum of aligned counts since the last worker start in this lane's range
+  int v = 0, f = 0;
+  for (int e = e0, l = e0 % Ef; e < e1; ++e, l = (l + 1 == Ef ? 0 : l + 1)) {
+    if (l == 0) {
+      v = 0;
+      f = 1;
+    }
+    v += align_up_dev(count_of(e), p.alpha);
+  }
+  // inclusive segmented scan over the lanes: (v, f) after (v', f') is
+  // (f ? v : v' + v, f | f')
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int vu = __shfl_up_sync(0xffffffffu, v, d);
+    const int fu = __shfl_up_sync(0xffffffffu, f, d);
+    if (lane >= d) {
+      if (!f) v += vu;
+      f |= fu;
+    }
+  }
+  int run = __shfl_up_sync(0xffffffffu, v, 1);  // running sum at the end of the previous lane
+  if (lane == 0) run = 0;
+  for (int e = e0, l = e0 % Ef; e < e1; ++e, l = (l + 1 == Ef ? 0 : l + 1)) {
+    if (l == 0) run = 0;
+    const int cnt = count_of(e);
+    const int al = align_up_dev(cnt, p.alpha);
+    sh_start[e] = run;
+    sh_end[e] = run + cnt;
+    if (out) {
+      p.starts[e] = run;
+      p.ends[e] = run + cnt;
+      p.hcounts[e] = al;
+    }
+    run += al;
+  }
+}
+
+// Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
+// or -1 for none). `pre` holds the row's first piece.
+__device__ __forceinline__ void copy_route(const DispatchParams& p, const SourceDesc& src, int t, int code,
+                                           const uint4 (&pre)[kScatterVecs]) {
+  if (code < 0) return;
+  const int lane = threadIdx.x & 31;
+  const int nvec = p.row_bytes >> 4;
+  const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
+  const int64_t r = (int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask);
+  uint4* dst = reinterpret_cast<uint4*>(p.rows + r * p.row_bytes);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
+    uint4 buf[kScatterVecs];
+    if (v0 == 0) {
+#pragma unroll
+      for (int j = 0; j < kScatterVecs; ++j) buf[j] = pre[j];
+    } else {
+      load_piece(buf, xrow, v0, nvec);
+    }
+#pragma unroll
+    for (int j = 0; j < kScatterVecs; ++j) {
+      const int v = v0 + j * 32 + lane;
+      if (v < nvec) dst[v] = buf[j];
+    }
+  }
+  for (int b = lane; b < p.nscale; b += 32)
+    p.row_scales[r * p.nscale + b] = src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
+}
+
+// At most 32 tokens in the whole exchange: one-warp blocks, one per (token,
+// route) pair (and at least 16, which share the padding rows). Every block
 // counts all the routes itself with one lane mask per expert (lane = token),
-// so ranks are popcounts of earlier lanes and no block-wide barrier is
-// needed; block b < N then scatters token b, and all blocks share the padding
-// rows.
+// so ranks are popcounts of earlier lanes and no block waits for another;
+// block b then writes the receipt of route b % K of token b / K and copies
+// the token's row there.
 __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(16) uint32_t tsm[];
   const int E = p.E, K = p.K, N = p.total_tokens;
@@ -539,68 +617,55 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   pdl_launch_dependents();
   const int lane = threadIdx.x;
 
+  // this block's route: token gt, route kk; its row, weight and ID load now
+  const bool has_pair = (int)blockIdx.x < N * K;
+  const int gt = has_pair ? (int)blockIdx.x / K : 0;
+  const int kk = (int)blockIdx.x - gt * K;
+  const int s = source_of_token(p, gt);
+  const SourceDesc& src = p.src[s];
+  const int t = gt - src.tok_off;
   uint4 pre[kScatterVecs];
-  float pre_w = 0.0f;
-  const bool has_token = preload_first(p, blockIdx.x, pre, pre_w);  // token blockIdx.x, if any
+  float w = 0.0f;
+  int64_t id = -1;
+  if (has_pair) {
+    load_piece(pre, reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes), 0, p.row_bytes >> 4);
+    if (lane == 0) {
+      w = src.w[(int64_t)t * K + kk];
+      id = src.ids[(int64_t)t * K + kk];
+    }
+  }
 
   for (int e = lane; e < E; e += 32) mask[e] = 0u;
   __syncwarp();
   uint32_t valid = 0u;
   if (lane < N) {
-    const int s = source_of_token(p, lane);
-    const int t = lane - p.src[s].tok_off;
-    valid = mark_token(p.src[s].ids + (int64_t)t * K, K, E, mask, lane, s, t,
+    const int ls = source_of_token(p, lane);
+    const int lt = lane - p.src[ls].tok_off;
+    valid = mark_token(p.src[ls].ids + (int64_t)lt * K, K, E, mask, lane, ls, lt,
                        blockIdx.x == 0 ? p.err : nullptr);
   }
   __syncwarp();
-  // aligned scan per worker, one warp
-  for (int f = 0; f < p.F; ++f) {
-    int carry = 0;
-    for (int l0 = 0; l0 < p.Ef; l0 += 32) {
-      const int l = l0 + lane;
-      const int e = f * p.Ef + l;
-      const int cnt = l < p.Ef ? __popc(mask[e]) : 0;
-      const int al = align_up_dev(cnt, p.alpha);
-      const int incl = warp_inclusive_scan(al);
-      if (l < p.Ef) {
-        const int start = carry + incl - al;
-        sh_start[e] = start;
-        sh_end[e] = start + cnt;
-        if (blockIdx.x == 0) {
-          p.starts[e] = start;
-          p.ends[e] = start + cnt;
-          p.hcounts[e] = al;
-        }
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
+  warp_worker_scan(p, [&](int e) { return __popc(mask[e]); }, sh_start, sh_end, blockIdx.x == 0);
   __syncwarp();
 
-  auto row_of = [&](int gt, int s, int t, int& e, int& row) -> bool {
-    if (!((__shfl_sync(0xffffffffu, valid, gt) >> lane) & 1u)) return false;
-    e = (int)p.src[s].ids[(int64_t)t * K + lane];
-    row = sh_start[e] + __popc(mask[e] & ((1u << gt) - 1u));
-    return true;
-  };
-  // the route rows of one token; all 32 lanes take part (the valid mask is
-  // gathered with a shuffle), lanes >= K only copy
-  const int gt = blockIdx.x;
-  if (has_token) {
-    const int s = source_of_token(p, gt);
-    const SourceDesc& src = p.src[s];
-    const int t = gt - src.tok_off;
-    int e = -1, row = 0;
-    const bool ok = row_of(gt, s, t, e, row);
+  if (has_pair) {
+    const bool ok = (__shfl_sync(0xffffffffu, valid, gt) >> kk) & 1u;
     int code = -1;
-    if (lane < K) {
+    if (lane == 0) {
       if (ok) {
-        code = write_route(p, s, t, gt, e, row, pre_w);
+        const int e = (int)id;
+        const int row = sh_start[e] + __popc(mask[e] & ((1u << gt) - 1u));
+        const int f = e / p.Ef;
+        const int64_t r = (int64_t)f * p.R_arena + row;
+        p.row_src[r] = (s * p.bucket + t) * K + kk;
+        p.row_w[r] = w;
+        code = (f << kWorkerShift) | row;
+        p.routes[(int64_t)gt * K + kk] = make_int2(code, __float_as_int(w));
       } else {
-        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+        p.routes[(int64_t)gt * K + kk] = make_int2(-1, 0);
       }
     }
-    copy_token<true>(p, src, t, code, pre);
+    copy_route(p, src, t, __shfl_sync(0xffffffffu, code, 0), pre);
   }
   // padding rows, spread over the blocks
   if (p.alpha > 1) {
@@ -701,8 +766,9 @@ cudaError_t configure_dispatch_kernels(int* max_ctas) {
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   const int block = 256;
   if (p.total_tokens >= 1 && p.total_tokens <= 32 && AFD_TINY_DISPATCH) {
-    // one block per token, and at least 16 blocks to share the padding rows
-    const int grid = p.total_tokens > 16 ? p.total_tokens : 16;
+    // one block per (token, route), and at least 16 blocks to share the padding rows
+    const int pairs = p.total_tokens * p.K;
+    const int grid = pairs > 16 ? pairs : 16;
     return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, true, p);
   }
   if (dispatch_is_small(p)) {
