@@ -541,7 +541,7 @@ def main():
         raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
     inp = W.make_inputs(wl)
     buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
-    buf_small = sum(wl.T) * wl.K <= 1024 or sum(wl.T) <= 32  # one-kernel dispatch (afd_dispatch.cu)
+    buf_small = sum(wl.T) * wl.K <= 2048 or sum(wl.T) <= 32  # one-kernel dispatch (afd_dispatch.cu)
 
     xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
           for s, T in enumerate(wl.T)]

@@ -389,6 +389,35 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   fill_padding(p, p.ends);
 }
 
+// Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
+// or -1 for none). kPre: `pre` holds the row's first piece.
+template <bool kPre>
+__device__ __forceinline__ void copy_route(const DispatchParams& p, const SourceDesc& src, int t, int code,
+                                           const uint4 (&pre)[kScatterVecs]) {
+  if (code < 0) return;
+  const int lane = threadIdx.x & 31;
+  const int nvec = p.row_bytes >> 4;
+  const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
+  const int64_t r = (int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask);
+  uint4* dst = reinterpret_cast<uint4*>(p.rows + r * p.row_bytes);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
+    uint4 buf[kScatterVecs];
+    if (kPre && v0 == 0) {
+#pragma unroll
+      for (int j = 0; j < kScatterVecs; ++j) buf[j] = pre[j];
+    } else {
+      load_piece(buf, xrow, v0, nvec);
+    }
+#pragma unroll
+    for (int j = 0; j < kScatterVecs; ++j) {
+      const int v = v0 + j * 32 + lane;
+      if (v < nvec) dst[v] = buf[j];
+    }
+  }
+  for (int b = lane; b < p.nscale; b += 32)
+    p.row_scales[r * p.nscale + b] = src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
+}
+
 // ---------------------------------------------------------------- small path
 
 __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_constant__ DispatchParams p) {
@@ -409,11 +438,16 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
 
-  // Load this warp's first row and weights now, so that their latency
-  // overlaps the counting below.
+  // Load this warp's first (token, route) pair's row and weight now, so that
+  // their latency overlaps the counting below.
   uint4 pre[kScatterVecs];
   float pre_w = 0.0f;
-  const bool have_pre = preload_first(p, gwarp, pre, pre_w);
+  const bool have_pre = gwarp < N * K;
+  if (have_pre) {
+    const int gt = gwarp / K, s = source_of_token(p, gt), t = gt - p.src[s].tok_off;
+    load_piece(pre, reinterpret_cast<const uint4*>(p.src[s].x + (int64_t)t * p.row_bytes), 0, p.row_bytes >> 4);
+    if (lane == 0) pre_w = p.src[s].w[(int64_t)t * K + (gwarp - gt * K)];
+  }
 
   // Pass 1 (every block, all routes): ranks inside each chunk, chunk counts.
   for (int c = 0; c < G; ++c) {
@@ -470,20 +504,35 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   worker_scan(p, sh_total, sh_start, blockIdx.x == 0);
   __syncthreads();
 
-  // Pass 2: this block's share of the tokens.
-  auto row_of = [&](int gt, int, int, int& e, int& row) -> bool {
-    const uint32_t info = rinfo[gt * K + lane];
-    if (info == ~0u) return false;
-    e = (int)(info >> kRankBits);
-    row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
-    return true;
-  };
-  int gt = gwarp;
-  if (have_pre) {
-    scatter_token<true>(p, gt, row_of, pre_w, pre);
-    gt += nwarps;
+  // Pass 2: a warp per (token, route) pair: the route's receipt and its row.
+  for (int pr = gwarp; pr < N * K; pr += nwarps) {
+    const int gt = pr / K, kk = pr - gt * K;
+    const int s = source_of_token(p, gt);
+    const SourceDesc& src = p.src[s];
+    const int t = gt - src.tok_off;
+    int code = -1;
+    if (lane == 0) {
+      const uint32_t info = rinfo[gt * K + kk];
+      const float w = pr == gwarp ? pre_w : src.w[(int64_t)t * K + kk];
+      if (info != ~0u) {
+        const int e = (int)(info >> kRankBits);
+        const int row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
+        const int f = e / p.Ef;
+        const int64_t r = (int64_t)f * p.R_arena + row;
+        p.row_src[r] = (s * p.bucket + t) * K + kk;
+        p.row_w[r] = w;
+        code = (f << kWorkerShift) | row;
+        p.routes[(int64_t)gt * K + kk] = make_int2(code, __float_as_int(w));
+      } else {
+        p.routes[(int64_t)gt * K + kk] = make_int2(-1, 0);
+      }
+    }
+    code = __shfl_sync(0xffffffffu, code, 0);
+    if (pr == gwarp)
+      copy_route<true>(p, src, t, code, pre);
+    else
+      copy_route<false>(p, src, t, code, pre);
   }
-  for (; gt < N; gt += nwarps) scatter_token<false>(p, gt, row_of, 0.0f, pre);
 
   // Padding rows, from this block's own copy of the layout.
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
@@ -573,34 +622,6 @@ __device__ __forceinline__ void warp_worker_scan(const DispatchParams& p, CountO
   }
 }
 
-// Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
-// or -1 for none). `pre` holds the row's first piece.
-__device__ __forceinline__ void copy_route(const DispatchParams& p, const SourceDesc& src, int t, int code,
-                                           const uint4 (&pre)[kScatterVecs]) {
-  if (code < 0) return;
-  const int lane = threadIdx.x & 31;
-  const int nvec = p.row_bytes >> 4;
-  const uint4* xrow = reinterpret_cast<const uint4*>(src.x + (int64_t)t * p.row_bytes);
-  const int64_t r = (int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask);
-  uint4* dst = reinterpret_cast<uint4*>(p.rows + r * p.row_bytes);
-  for (int v0 = 0; v0 < nvec; v0 += 32 * kScatterVecs) {
-    uint4 buf[kScatterVecs];
-    if (v0 == 0) {
-#pragma unroll
-      for (int j = 0; j < kScatterVecs; ++j) buf[j] = pre[j];
-    } else {
-      load_piece(buf, xrow, v0, nvec);
-    }
-#pragma unroll
-    for (int j = 0; j < kScatterVecs; ++j) {
-      const int v = v0 + j * 32 + lane;
-      if (v < nvec) dst[v] = buf[j];
-    }
-  }
-  for (int b = lane; b < p.nscale; b += 32)
-    p.row_scales[r * p.nscale + b] = src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
-}
-
 // At most 32 tokens in the whole exchange: one-warp blocks, one per (token,
 // route) pair (and at least 16, which share the padding rows). Every block
 // counts all the routes itself with one lane mask per expert (lane = token),
@@ -665,7 +686,7 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
         p.routes[(int64_t)gt * K + kk] = make_int2(-1, 0);
       }
     }
-    copy_route(p, src, t, __shfl_sync(0xffffffffu, code, 0), pre);
+    copy_route<true>(p, src, t, __shfl_sync(0xffffffffu, code, 0), pre);
   }
   // padding rows, spread over the blocks
   if (p.alpha > 1) {
@@ -772,7 +793,7 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
     return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, true, p);
   }
   if (dispatch_is_small(p)) {
-    int grid = (p.total_tokens + 7) / 8;
+    int grid = (p.total_tokens * p.K + 7) / 8;  // a warp per (token, route)
     if (grid > sm_cap) grid = sm_cap;
     if (grid < 1) grid = 1;
     return launch(dispatch_small_kernel, grid, block, small_smem(p.E, p.total_tokens, p.K), stream,

@@ -18,7 +18,7 @@ constexpr int32_t kRowMask = (1 << kWorkerShift) - 1;
 constexpr int kLayoutMaxCtas = 16;   // largest layout cluster
 constexpr int kRankBits = 8;         // one-kernel dispatch code = (expert << 8) | rank in chunk
 #ifndef AFD_SMALL_ROUTES
-#define AFD_SMALL_ROUTES 1024         // exchanges up to this many routes take the one-kernel dispatch
+#define AFD_SMALL_ROUTES 2048         // exchanges up to this many routes take the one-kernel dispatch
 #endif
 constexpr int kSmallRoutes = AFD_SMALL_ROUTES;
 constexpr int kSmallSmemMax = 110 * 1024;

@@ -191,14 +191,14 @@ def test_edge_cases():
         W.Workload("a=5", A=5, F=2, E=32, K=6, H=1024, alpha=16, capacity=200, bucket=160,
                    T=(160, 0, 77, 1, 159)),
         # the one-warp dispatch takes up to 32 tokens, the one-kernel dispatch up
-        # to 1024 routes; both sides of each switch
+        # to 2048 routes; both sides of each switch
         W.Workload("tiny-max", A=1, F=2, E=64, K=8, H=512, alpha=8, capacity=40, bucket=40, T=(32,)),
         W.Workload("tiny-max+1", A=1, F=2, E=64, K=8, H=512, alpha=8, capacity=40, bucket=40, T=(33,)),
         W.Workload("tiny-3src", A=3, F=3, E=96, K=32, H=256, alpha=128, capacity=16, bucket=16, T=(11, 0, 9)),
         W.Workload("small-max", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
-                   T=(1024,)),
+                   T=(2048,)),
         W.Workload("small-max+1", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
-                   T=(1025,)),
+                   T=(2049,)),
         W.Workload("cluster-16x256", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
                    T=(4096,)),
         W.Workload("large-min", A=1, F=2, E=8, K=1, H=256, alpha=1, capacity=4097, bucket=4097,
