@@ -378,6 +378,20 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
               : launch_pdl(combine_kernel<1>, grid, 256, stream, p);
 }
 
+cudaError_t configure_combine_kernels() {
+  cudaError_t e = cudaSuccess;
+  for (const void* k : {(const void*)combine_token_kernel<AFD_COMBINE_FUSED>,
+                        (const void*)combine_token_kernel<AFD_COMBINE_TWO_STAGE>,
+                        (const void*)combine_token_kernel<AFD_COMBINE_TWO_STAGE_FP8>,
+                        (const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>,
+                        (const void*)copy_kernel})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
+  return e;
+}
+
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
   const int64_t total = (int64_t)p.rows * (p.H >> 3);
   if (total <= 0) return cudaSuccess;

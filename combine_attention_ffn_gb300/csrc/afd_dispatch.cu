@@ -175,43 +175,35 @@ __device__ __forceinline__ void copy_token(const DispatchParams& p, const Source
   }
 }
 
-// Writes route (s, t, lane)'s receipt entries for a final row and returns its
-// route code. Called by lanes < K.
-__device__ __forceinline__ int write_route(const DispatchParams& p, int s, int t, int gt, int e,
-                                           int row, float w) {
-  const int f = e / p.Ef;
+// Writes route (s, t, lane)'s receipt entries for its final code
+// ((worker << 24) | row). Called by lanes < K.
+__device__ __forceinline__ void write_route(const DispatchParams& p, int s, int t, int gt, int code, float w) {
   const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)f * p.R_arena + row;
+  const int64_t r = (int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask);
   p.row_src[r] = (s * p.bucket + t) * p.K + lane;
   p.row_w[r] = w;
-  const int code = (f << kWorkerShift) | row;
   p.routes[(int64_t)gt * p.K + lane] = make_int2(code, __float_as_int(w));
-  return code;
 }
 
-// One token of the scatter: finish each route's row from the layout (the
-// chunk's first row of the expert plus the route's rank inside the chunk),
-// write the receipt, copy the row. kPre: the row's first piece and the
-// weights were loaded early into pre / pre_w.
-template <bool kPre, typename RowOf>
-__device__ __forceinline__ void scatter_token(const DispatchParams& p, int gt, RowOf row_of,
-                                              float pre_w, const uint4 (&pre)[kScatterVecs]) {
+// One token of the scatter: lane k < K holds route k's final code from the
+// layout ((worker << 24) | row, or -1). Writes the receipt and copies the
+// row. kPre: the row's first piece and the weights were loaded early into
+// pre / pre_w.
+template <bool kPre>
+__device__ __forceinline__ void scatter_token(const DispatchParams& p, int gt, int code, float pre_w,
+                                              const uint4 (&pre)[kScatterVecs]) {
   const int lane = threadIdx.x & 31;
   const int K = p.K;
   const int s = source_of_token(p, gt);
   const SourceDesc& src = p.src[s];
   const int t = gt - src.tok_off;
-  int code = -1;
   if (lane < K) {
-    int e = -1, row = 0;
-    if (row_of(gt, s, t, e, row)) {
-      const float w = kPre ? pre_w : src.w[(int64_t)t * K + lane];
-      code = write_route(p, s, t, gt, e, row, w);
-    } else {
+    if (code >= 0)
+      write_route(p, s, t, gt, code, kPre ? pre_w : src.w[(int64_t)t * K + lane]);
+    else
       p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
-    }
   }
-  copy_token<kPre>(p, src, t, code, pre);
+  copy_token<kPre>(p, src, t, lane < K ? code : -1, pre);
 }
 
 // Loads warp `gwarp`'s first token's first row piece and weights.
@@ -233,16 +225,17 @@ __device__ __forceinline__ bool preload_first(const DispatchParams& p, int gwarp
 // the tokens [r * tpc, (r + 1) * tpc) of the flattened (source, token) order
 // (tpc = ceil(N / n)) in slices of 256, keeping a running count per expert in
 // its shared memory, and gives each valid route its rank among the CTA's
-// routes to the same expert. After a cluster barrier every CTA reads all n
-// count vectors through distributed shared memory, so each one computes the
-// totals, the aligned per-worker scan and the first row of its own run of
-// each expert (start[e] plus the counts of CTAs r' < r) without a
-// global-memory round trip. A route's final row is that base plus its rank;
-// the scatter kernel, spread over every SM, adds them up and writes the
-// receipts. Because the CTAs hold consecutive token ranges and ranks follow
-// token order inside a CTA, rows inside an expert follow (source, token)
-// order.
-constexpr int kLocalRankBits = 21;  // layout code = (expert << 21) | rank in the CTA
+// routes to the same expert (kept in shared memory). After a cluster barrier
+// every CTA reads all n count vectors through distributed shared memory, so
+// each one computes the totals, the aligned per-worker scan and the first
+// row of its own run of each expert (start[e] plus the counts of CTAs
+// r' < r) without a global-memory round trip, and writes its routes' final
+// codes: (worker << 24) | (that first row + rank). The scatter kernel,
+// spread over every SM, writes the receipts from them. Because the CTAs hold
+// consecutive token ranges and ranks follow token order inside a CTA, rows
+// inside an expert follow (source, token) order.
+constexpr int kLocalRankBits = 21;  // local code = (expert << 21) | rank in the CTA
+constexpr int kLayoutCodesMax = 8192;  // local codes a CTA keeps in shared memory (32 KB)
 
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -280,6 +273,7 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
   int32_t* total = cnt + E;                                     // [E]
   int32_t* start = total + E;                                   // [E]
   int32_t* before = start + E;                                  // [E] counts of earlier CTAs
+  int32_t* codes_sm = before + E;                               // [tpc * K] when they fit
   // The first kernel of an exchange is a programmatic dependent of whatever
   // ran before it on the stream: it waits for that work (which may produce
   // the IDs, weights and rows, or still read the arenas) before touching
@@ -293,21 +287,25 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
   const int lo = min(N, (int)r * tpc), hi = min(N, lo + tpc);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lanes_before = (1u << lane) - 1u;
+  // each route's (expert, rank in this CTA) until the scan gives its row: in
+  // shared memory when they fit, else in the route-code scratch itself
+  int32_t* codes = (int64_t)tpc * K <= kLayoutCodesMax ? codes_sm : p.route_tmp + (int64_t)lo * K;
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   for (int c0 = lo; c0 < hi; c0 += kChunk) {
-    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
-    __syncthreads();
     const int gt = c0 + threadIdx.x;
     const bool live = gt < hi;
-    const int64_t* ids = nullptr;
-    uint32_t valid = 0u;
+    int s = 0, t = 0;
     if (live) {
-      const int s = source_of_token(p, gt);
-      const int t = gt - p.src[s].tok_off;
-      ids = p.src[s].ids + (int64_t)t * K;
-      valid = mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err);
+      s = source_of_token(p, gt);
+      t = gt - p.src[s].tok_off;
+      // start the IDs' first read while the masks are cleared
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p.src[s].ids + (int64_t)t * K));
     }
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
+    __syncthreads();
+    const int64_t* ids = p.src[s].ids + (int64_t)t * K;
+    const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err) : 0u;
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       int run = cnt[e];
@@ -320,14 +318,14 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
     }
     __syncthreads();
     if (live) {
-      int32_t* rt = p.route_tmp + (int64_t)gt * K;
+      int32_t* mine = codes + (int64_t)(gt - lo) * K;
       for (int k = 0; k < K; ++k) {
         int code = -1;
         if ((valid >> k) & 1u) {
           const int e = (int)ids[k];
           code = (e << kLocalRankBits) | (wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before));
         }
-        rt[k] = code;
+        mine[k] = code;
       }
     }
     __syncthreads();  // the masks are cleared for the next slice
@@ -354,7 +352,18 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
   __syncthreads();
   worker_scan(p, total, start, r == 0);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) p.cta_base[r * E + e] = start[e] + before[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) start[e] += before[e];  // this CTA's first row
+  __syncthreads();
+  // every route's final code: (worker << 24) | row, or -1
+  for (int i = threadIdx.x; i < (hi - lo) * K; i += blockDim.x) {
+    const int c = codes[i];
+    int code = -1;
+    if (c >= 0) {
+      const int e = c >> kLocalRankBits;
+      code = ((e / p.Ef) << kWorkerShift) | (start[e] + (c & ((1 << kLocalRankBits) - 1)));
+    }
+    p.route_tmp[(int64_t)lo * K + i] = code;
+  }
   cluster_wait();
 }
 
@@ -363,8 +372,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, E = p.E;
-  const int tpc = layout_tpc(p);
+  const int K = p.K;
 
   // The source rows and weights are inputs, not layout outputs: start loading
   // this warp's first token while the layout kernel is still running.
@@ -373,19 +381,13 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   const bool have_pre = preload_first(p, gwarp, pre, pre_w);
   pdl_wait();  // the layout kernel's outputs
 
-  auto row_of = [&](int gt, int, int, int& e, int& row) -> bool {
-    const int code = __ldcg(p.route_tmp + (int64_t)gt * K + lane);
-    if (code < 0) return false;
-    e = code >> kLocalRankBits;
-    row = __ldcg(p.cta_base + (gt / tpc) * E + e) + (code & ((1 << kLocalRankBits) - 1));
-    return true;
-  };
+  auto code_of = [&](int gt) { return lane < K ? __ldcg(p.route_tmp + (int64_t)gt * K + lane) : -1; };
   int gt = gwarp;
   if (have_pre) {
-    scatter_token<true>(p, gt, row_of, pre_w, pre);
+    scatter_token<true>(p, gt, code_of(gt), pre_w, pre);
     gt += nwarps;
   }
-  for (; gt < p.total_tokens; gt += nwarps) scatter_token<false>(p, gt, row_of, 0.0f, pre);
+  for (; gt < p.total_tokens; gt += nwarps) scatter_token<false>(p, gt, code_of(gt), 0.0f, pre);
   fill_padding(p, p.ends);
 }
 
@@ -702,7 +704,7 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   }
 }
 
-size_t layout_smem(int E) { return (size_t)kChunkWarps * E * 8 + (size_t)4 * E * 4; }
+size_t layout_smem(int E) { return (size_t)kChunkWarps * E * 8 + (size_t)4 * E * 4 + (size_t)kLayoutCodesMax * 4; }
 
 
 size_t small_smem(int E, int N, int K) {
@@ -751,6 +753,11 @@ cudaError_t configure_dispatch_kernels(int* max_ctas) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
+  for (const void* k : {(const void*)cluster_layout_kernel, (const void*)scatter_kernel,
+                        (const void*)dispatch_small_kernel, (const void*)dispatch_tiny_kernel,
+                        (const void*)cached_scatter_kernel})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
   if (e != cudaSuccess) return e;
   // the largest cluster that fits with the largest shared-memory request
   for (int n = kLayoutMaxCtas; n >= 1; n /= 2) {

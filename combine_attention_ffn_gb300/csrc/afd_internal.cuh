@@ -41,6 +41,14 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #endif
 static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 
+// Every kernel of the library asks for the same split of each SM's unified
+// L1 / shared memory. The kernels of one exchange overlap on the same SMs
+// through programmatic dependent launch; when their preferred splits differ
+// (the layout needs tens of KB of shared memory, the copy kernels none), an
+// SM cannot take blocks of the next kernel until it has drained and changed
+// its split, which cost up to 6 us per round trip.
+constexpr int kSharedCarveout = 50;  // percent of the maximum shared memory
+
 constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
 constexpr int kErrDup = 6;    // AFD_ERR_ROUTE_DUP
 constexpr unsigned long long kNoError = ~0ull;
@@ -72,8 +80,7 @@ struct DispatchParams {
   int32_t layout_ctas;   // CTAs of the layout cluster (large path)
   int64_t R_arena;       // rows per worker arena
   // context scratch
-  int32_t* route_tmp;    // [total_tokens][K]: (expert << 21) | rank among the layout CTA's routes, or -1
-  int32_t* cta_base;     // [kLayoutMaxCtas][E]: first row of each layout CTA's run of expert e
+  int32_t* route_tmp;    // [total_tokens][K]: the layout's route codes, (worker << 24) | row, or -1
   unsigned long long* err;
   // context outputs
   int32_t* starts;       // [E] aligned start of each expert (worker-local rows)
@@ -111,5 +118,6 @@ cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStrea
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t configure_dispatch_kernels(int* max_ctas);
+cudaError_t configure_combine_kernels();
 
 }  // namespace afd

@@ -54,7 +54,6 @@ struct afd_ctx {
   int32_t* hcounts;
   int2* routes;
   int32_t* route_tmp;
-  int32_t* cta_base;
   unsigned long long* err;
   uint16_t* inbox;
   // pinned host
@@ -221,7 +220,6 @@ void free_all(afd_ctx* c) {
   cudaFree(c->hcounts);
   cudaFree(c->routes);
   cudaFree(c->route_tmp);
-  cudaFree(c->cta_base);
   cudaFree(c->err);
   cudaFree(c->inbox);
   cudaFreeHost(c->host_counts);
@@ -286,7 +284,6 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   p.total_tokens = tok;
   p.R_arena = c->R_arena;
   p.route_tmp = c->route_tmp;
-  p.cta_base = c->cta_base;
   p.layout_ctas = afd::layout_ctas_for(tok, c->sm_cap, c->layout_max_ctas);
   p.err = c->err;
   p.starts = c->starts;
@@ -391,7 +388,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
             dev_alloc(&c->hcounts, (size_t)E) &&
             dev_alloc(&c->routes, (size_t)(A * g.capacity * K)) &&
             dev_alloc(&c->route_tmp, (size_t)(A * g.capacity * K)) &&
-            dev_alloc(&c->cta_base, (size_t)(afd::kLayoutMaxCtas * E)) && dev_alloc(&c->err, 1);
+            dev_alloc(&c->err, 1);
   if (ok && c->nscale) ok = dev_alloc(&c->row_scales, (size_t)(F * c->R_arena * c->nscale));
   if (ok && F == 1) ok = dev_alloc(&c->inbox, (size_t)(A * g.capacity * g.hidden));
   if (ok) ok = cudaMallocHost(reinterpret_cast<void**>(&c->host_counts), E * sizeof(int32_t)) == cudaSuccess;
@@ -407,6 +404,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->row_src, 0xff, (size_t)(F * c->R_arena) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->row_w, 0, (size_t)(F * c->R_arena) * sizeof(float));
   if (e == cudaSuccess) e = afd::configure_dispatch_kernels(&c->layout_max_ctas);
+  if (e == cudaSuccess) e = afd::configure_combine_kernels();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     fprintf(stderr, "afd_create: %s\n", cudaGetErrorString(e));
