@@ -16,15 +16,18 @@
 // count of earlier warps' tokens plus the popcount of the earlier lanes of
 // its own mask. A repeated ID shows up as a mask bit that is already set.
 //
-// Two paths:
-//  * small exchanges (at most kSmallRoutes routes): one kernel. Every block
-//    counts all routes itself (they are few and sit in L2), scans in shared
-//    memory, then copies its share of the rows. No block waits for another.
-//  * large exchanges: cluster_layout_kernel (one thread-block cluster; the
+// Three paths:
+//  * at most 32 tokens: dispatch_tiny_kernel, one-warp blocks, one per
+//    (token, route); a lane per token counts with one mask word per expert.
+//  * at most kSmallRoutes routes: dispatch_small_kernel, one kernel, a warp
+//    per (token, route). Every block counts all routes itself (they are few
+//    and sit in L2) and scans in shared memory; no block waits for another.
+//  * larger exchanges: cluster_layout_kernel (one thread-block cluster; the
 //    CTAs share their counts through distributed shared memory and write
-//    every route's final row) then scatter_kernel (a warp per token),
-//    launched as a programmatic dependent: its blocks start early and load
-//    their first source rows while the layout is still running.
+//    every route's final code) then scatter_kernel (a warp per token, which
+//    reads its row once and writes it to each route), launched as a
+//    programmatic dependent: its blocks start early and load their first
+//    source rows while the layout is still running.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
