@@ -690,7 +690,7 @@ def main():
     n_launch = wl.A if wl.F > 1 else 1
     per_launch_s = comb_ms / n_launch * 1e-3
     per_launch_bytes = ab["combine"] / n_launch
-    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 8 * 152 else "combine_kernel"
+    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * 152 else "combine_kernel"
     achieved = per_launch_bytes / per_launch_s / 1e9
     traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}")
     d_gbs = ab["dispatch"] / (d_ms * 1e-3) / 1e9

@@ -37,7 +37,7 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #define AFD_TWO_STAGE_BLOCKS 7    // resident two-warp blocks per SM asked of the two-stage per-token combine
 #endif
 #ifndef AFD_TOKEN_COMBINE_MIN
-#define AFD_TOKEN_COMBINE_MIN 8  // x SMs: tokens from which the per-token combine is used
+#define AFD_TOKEN_COMBINE_MIN 4  // x SMs: tokens from which the per-token combine is used
 #endif
 static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 

@@ -49,7 +49,7 @@ def _roundtrip_check(wl, mode=GH.SCALE, rhc=False, view=False, transposed=False,
 
 CASES = (
     [("tiny", None)]
-    + [("2A2F", T) for T in (1, 8, 32, 128, 512, 2048)]
+    + [("2A2F", T) for T in (1, 8, 32, 128, 512, 607, 608, 2048)]  # 608 = 4 tokens per SM: per-token combine
     + [("2A2F-H4096", T) for T in (1, 128, 2048)]
     + [("skew-3A1F", T) for T in (1, 32, 512, 2048)]
     + [("skew-1A3F", T) for T in (1, 32, 512, 2048)]
