@@ -355,17 +355,14 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
   __syncthreads();
   worker_scan(p, total, start, r == 0);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) start[e] += before[e];  // this CTA's first row
+  // this CTA's first code per expert: (worker << 24) | its first row
+  for (int e = threadIdx.x; e < E; e += blockDim.x) start[e] = ((e / p.Ef) << kWorkerShift) + start[e] + before[e];
   __syncthreads();
   // every route's final code: (worker << 24) | row, or -1
   for (int i = threadIdx.x; i < (hi - lo) * K; i += blockDim.x) {
     const int c = codes[i];
-    int code = -1;
-    if (c >= 0) {
-      const int e = c >> kLocalRankBits;
-      code = ((e / p.Ef) << kWorkerShift) | (start[e] + (c & ((1 << kLocalRankBits) - 1)));
-    }
-    p.route_tmp[(int64_t)lo * K + i] = code;
+    p.route_tmp[(int64_t)lo * K + i] =
+        c < 0 ? -1 : start[c >> kLocalRankBits] + (c & ((1 << kLocalRankBits) - 1));
   }
   cluster_wait();
 }
