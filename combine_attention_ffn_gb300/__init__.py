@@ -8,7 +8,8 @@ inputs. Importing this package does not load the CUDA library: the first use
 of :class:`Buffer` does, and fails loudly if it has not been built.
 """
 
-__all__ = ["Buffer", "AfdError", "load_library"]
+__all__ = ["Buffer", "AfdError", "load_library", "route_layout_noalloc",
+           "COMBINE_FUSED", "COMBINE_TWO_STAGE", "COMBINE_TWO_STAGE_FP8"]
 
 
 def __getattr__(name):

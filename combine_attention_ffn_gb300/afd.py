@@ -349,6 +349,12 @@ class Buffer:
     def reset_exchange(self) -> None:
         self._check(self._lib.afd_reset_exchange(self._h), "reset_exchange")
 
+    def __enter__(self) -> "Buffer":
+        return self
+
+    def __exit__(self, *exc) -> None:
+        self.close()
+
     def close(self) -> None:
         """Releases the context. Its memory is freed (after the device work
         completes) once no tensor viewing it is alive."""
