@@ -97,8 +97,8 @@ enum { AFD_BF16 = 0, AFD_FP8_E4M3 = 1 };
  * The two-stage modes need top_k <= 8. */
 enum { AFD_COMBINE_FUSED = 0, AFD_COMBINE_TWO_STAGE = 1, AFD_COMBINE_TWO_STAGE_FP8 = 2 };
 
-/* Fixed per context. "API contract", Roles and tensors: H is a multiple of
- * 256, K <= min(32, E), experts divide evenly over the workers (worker f owns
+/* Fixed per context. "API contract", Roles and tensors: H divisible by 256,
+ * top-k at most 32 and at most E, experts divide evenly over the workers (worker f owns
  * experts [f*E/F, (f+1)*E/F)). Limits of this build: A <= 64, F <= 64,
  * E <= 1024, and a worker arena below 2^24 rows. */
 typedef struct afd_config {

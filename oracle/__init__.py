@@ -20,7 +20,7 @@ What each function follows (afdEP-comm pages):
   selected experts in token order, weight applied once) and design page
   section 19 (FP32 sum in slot order, one rounding to BF16).
 * ``combine_two_stage`` -- design page sections 6 and 19: per-worker BF16
-  partials (optionally E4M3 with a power-of-two scale per 128 elements),
+  partials (optionally E4M3 with one power-of-two factor shared by each block of 128 values),
   summed in FP32 in the order of each worker's last route, rounded once.
 
 Parity pins for each of these live in ``tests/test_oracle_*.py``.

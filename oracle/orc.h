@@ -100,7 +100,7 @@ void orc_group_exponent_n(const float* amax, int32_t* out, int64_t n);
 /* Two-stage combine (design page, sections 6 and 19): for every token, each
  * worker's routes give a BF16 partial (FP32 fused multiply-adds in ascending
  * k from +0, one rounding); with fp8 != 0 each partial is quantized to E4M3
- * with one power-of-two scale per 128 elements and dequantized; the partials
+ * with one power-of-two factor shared by each block of 128 values, and dequantized; the partials
  * are added in FP32 in the order of each worker's last route (ascending k),
  * from +0, and the sum is rounded once to BF16. */
 void orc_combine_two_stage(const orc_problem* p, const int64_t* ids, const float* w,

@@ -1,5 +1,5 @@
 """The two-stage combine modes (per-worker BF16 partials, optionally FP8
-partials with a power-of-two scale per 128 elements) against the oracle, bit
+partials with one power-of-two factor shared by each block of 128 values) against the oracle, bit
 for bit."""
 import numpy as np
 import pytest
