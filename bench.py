@@ -535,7 +535,11 @@ def main():
     from combine_attention_ffn_gb300 import build as libbuild
     from combine_attention_ffn_gb300 import workloads as W
 
-    libbuild.build()
+    # one rank builds (if the sources are newer than the library), the others wait
+    if rank == 0:
+        libbuild.build()
+    if ws > 1:
+        torch.distributed.barrier()
     wl = W.named(args.config, T=args.tokens)
     if wl.dtype == "fp8":
         raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
