@@ -9,12 +9,19 @@
 //   out = bf16_round_nearest_even(acc)
 // so the result does not depend on the launch shape.
 //
-// Work items are (token, segment): a segment is U x 32 consecutive 16-byte
-// slices of the hidden row, one slice per lane per step (8 BF16 each). A
-// warp takes one item at a time, issues the loads of up to 8 routes at once
-// and then their FMAs in ascending k. Splitting a token's row into segments
-// spreads a few tokens over many warps ("R2" of the afdEP-comm design page
-// spreads few-token combines the same way) and balances large batches.
+// Two kernels compute it:
+//  * combine_token_kernel (K <= 8, at least 4 tokens per SM): a warp per
+//    token walks the row in 512-byte segments with a two-stage register
+//    pipeline (the next segment's loads, one per route, are in flight while
+//    the current one is summed and stored).
+//  * combine_kernel<U> (fewer tokens, or K > 8): work items are (token,
+//    segment), a segment being U x 32 consecutive 16-byte slices of the row;
+//    a warp issues the loads of up to 8 routes at once, then their FMAs in
+//    ascending k. Splitting a token's row into segments spreads a few tokens
+//    over many warps ("R2" of the afdEP-comm design page spreads few-token
+//    combines the same way).
+// The two-stage modes (design page section 19) use the same two kernels
+// with per-worker partials (combine_two_stage_kernel is the segmented one).
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
