@@ -145,7 +145,7 @@ def _wrap(ptr, shape, dtype: torch.dtype, owner, device) -> torch.Tensor:
 
 
 def _stream_handle(stream, device) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream(device)
+    s = stream if stream is not None else torch.cuda.current_stream(device.index)
     return int(s.cuda_stream)
 
 
@@ -188,6 +188,7 @@ class Buffer:
             raise AfdError(st, "afd_create: " + self._lib.afd_status_string(st).decode())
         self._ctx = _Context(self._lib, h)
         self._h = h
+        self._views = {}
 
     # the dtype the top-k IDs must have ("API contract": buffer.topk_idx_dtype)
     topk_idx_dtype = torch.int64
@@ -197,6 +198,18 @@ class Buffer:
         if st != OK:
             detail = self._lib.afd_error_detail(self._h).decode() if self._h else ""
             raise AfdError(st, f"{what}: {self._lib.afd_status_string(st).decode()}: {detail}")
+
+    def _view(self, ptr, shape, dtype: torch.dtype) -> torch.Tensor:
+        """A tensor over context-owned memory. The arenas never move, so the
+        tensors are made once per (address, shape, dtype) and reused."""
+        key = (int(ptr or 0), tuple(shape), dtype)
+        t = self._views.get(key)
+        if t is None:
+            if len(self._views) >= 256:  # exact receive shapes vary with read_host_counts
+                self._views.clear()
+            t = _wrap(ptr, shape, dtype, self._ctx, self.device)
+            self._views[key] = t
+        return t
 
     @property
     def handle(self) -> int:
@@ -273,12 +286,11 @@ class Buffer:
             hc = np.ctypeslib.as_array(ctypes.cast(r.host_counts, ctypes.POINTER(ctypes.c_int32)),
                                        shape=(self.Ef,)).copy()
         return Receive(
-            rows=_wrap(r.rows, (n, self.H), rows_dtype, self._ctx, self.device),
-            row_scales=(_wrap(r.row_scales, (n, self.H // 128), torch.float32, self._ctx, self.device)
-                        if r.row_scales else None),
-            weights=_wrap(r.weights, (n,), torch.float32, self._ctx, self.device),
-            row_src=_wrap(r.row_src, (n,), torch.int32, self._ctx, self.device),
-            ends=_wrap(r.ends, (self.Ef,), torch.int32, self._ctx, self.device),
+            rows=self._view(r.rows, (n, self.H), rows_dtype),
+            row_scales=self._view(r.row_scales, (n, self.H // 128), torch.float32) if r.row_scales else None,
+            weights=self._view(r.weights, (n,), torch.float32),
+            row_src=self._view(r.row_src, (n,), torch.int32),
+            ends=self._view(r.ends, (self.Ef,), torch.int32),
             host_counts=hc, num_rows=n, receipt=int(r.receipt))
 
     def worker_reply(self, worker: int, rows: torch.Tensor, receipt: int, stream=None) -> None:
@@ -302,9 +314,7 @@ class Buffer:
                                           _stream_handle(stream, self.device), ctypes.byref(v))
         self._check(st, "source_collect")
         if v.is_view:
-            T = int(v.num_tokens)
-            base = _wrap(v.data, (T, int(v.row_stride)), torch.bfloat16, self._ctx, self.device)
-            return base[:, : self.H]
+            return self._view(v.data, (int(v.num_tokens), int(v.row_stride)), torch.bfloat16)[:, : self.H]
         return out
 
     def source_collect_all(self, *, view: bool = False, outs=None, num_tokens=None, stream=None):
@@ -327,9 +337,7 @@ class Buffer:
         for s in range(self.A):
             v = views[s]
             if v.is_view:
-                T = int(v.num_tokens)
-                res.append(_wrap(v.data, (T, int(v.row_stride)), torch.bfloat16, self._ctx,
-                                 self.device)[:, : self.H])
+                res.append(self._view(v.data, (int(v.num_tokens), int(v.row_stride)), torch.bfloat16)[:, : self.H])
             else:
                 res.append(outs[s])
         return res
@@ -358,6 +366,7 @@ class Buffer:
     def close(self) -> None:
         """Releases the context. Its memory is freed (after the device work
         completes) once no tensor viewing it is alive."""
+        self._views = {}
         self._ctx = None
         self._h = ctypes.c_void_p()
 
