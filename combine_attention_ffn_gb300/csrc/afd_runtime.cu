@@ -179,6 +179,10 @@ afd_status order_stream(afd_ctx* c, cudaStream_t s) {
   return AFD_OK;
 }
 
+// Every call records the mark, even one that enqueued nothing: the mark also
+// covers the caller's own work before the call on that stream (the expert
+// before worker_reply, the producer of x before source_dispatch), which a
+// later call on another stream must wait for.
 afd_status mark_stream(afd_ctx* c, cudaStream_t s) {
   cudaError_t e = cudaEventRecord(c->order_ev, s);
   if (e != cudaSuccess) return cuda_fail(c, e, "cudaEventRecord");
