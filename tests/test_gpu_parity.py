@@ -260,10 +260,46 @@ def test_roles_on_separate_streams():
                 buf.source_dispatch(s, dev.x[s], dev.ids[s], dev.w[s], bucket=wl.bucket)
         with torch.cuda.stream(s2):
             recvs = {f: buf.worker_receive(f, bucket=wl.bucket) for f in range(wl.F)}
+            replies = {f: GH.expert_reply(wl, f, recvs[f], GH.SCALE) for f in range(wl.F)}
             for f in range(wl.F):
-                rep = GH.expert_reply(wl, f, recvs[f], GH.SCALE)
-                buf.worker_reply(f, rep, recvs[f].receipt)
+                buf.worker_reply(f, replies[f], recvs[f].receipt)
         with torch.cuda.stream(s3):
+            outs = GH.alloc_outs(wl)
+            res = [buf.source_collect(s, out=outs[s]) for s in range(wl.A)]
+        torch.cuda.synchronize()
+        GH.check_layout(wl, GH.snapshot(recvs), exp, False, buf)
+        GH.check_outputs(wl, res, exp)
+    finally:
+        buf.close()
+
+
+def test_calls_on_another_stream_wait_for_the_callers_work():
+    """A call on a new stream waits for everything enqueued before the previous
+    call on the old stream, including the caller's own kernels: a slow producer
+    of x before source 0's dispatch on one stream, the last dispatch on
+    another; a slow expert before the replies on one stream, the collects on
+    another. Each slow kernel spins a fixed number of cycles first."""
+    wl = W.named("2A2F", T=512)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE)
+    buf = GH.make_buffer(wl)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        dev = GH.to_device(inp)
+        x0 = torch.zeros_like(dev.x[0])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            torch.cuda._sleep(2_000_000)  # about a millisecond
+            x0.copy_(dev.x[0])            # the producer of source 0's rows
+            buf.source_dispatch(0, x0, dev.ids[0], dev.w[0], bucket=wl.bucket)
+        with torch.cuda.stream(s2):
+            buf.source_dispatch(1, dev.x[1], dev.ids[1], dev.w[1], bucket=wl.bucket)
+            recvs = {f: buf.worker_receive(f, bucket=wl.bucket) for f in range(wl.F)}
+            torch.cuda._sleep(2_000_000)
+            replies = {f: GH.expert_reply(wl, f, recvs[f], GH.SCALE) for f in range(wl.F)}
+            for f in range(wl.F):
+                buf.worker_reply(f, replies[f], recvs[f].receipt)
+        with torch.cuda.stream(s1):
             outs = GH.alloc_outs(wl)
             res = [buf.source_collect(s, out=outs[s]) for s in range(wl.A)]
         torch.cuda.synchronize()
