@@ -78,3 +78,36 @@ def test_random_exchange_matches_oracle(seed):
         GH.check_outputs(wl, res2, exp2)
     finally:
         buf.close()
+
+
+def _draw_large(seed: int):
+    rng = random.Random(7000 + seed)
+    F = rng.choice([1, 2, 3, 4])
+    E = F * rng.choice([16, 32, 64])
+    K = rng.choice([4, 6, 8])
+    A = rng.randint(1, 3)
+    H = rng.choice([2048, 4096])
+    T = tuple(rng.choice([rng.randint(600, 2048), 2048]) for _ in range(A))
+    dtype = "fp8" if rng.random() < 0.3 else "bf16"
+    mode = rng.choice([0, 0, 1, 2])
+    wl = W.Workload(f"fuzz-large{seed}", A=A, F=F, E=E, K=K, H=H, alpha=rng.choice([1, 64, 128]),
+                    capacity=2048, bucket=2048, T=T, dtype=dtype,
+                    routing=rng.choice(["uniform", "zipf"]), drop=rng.choice([0.0, 0.1]), seed=2000 + seed)
+    return wl, mode
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_large_exchange_matches_oracle(seed):
+    """Production-sized random exchanges (H 2048 or 4096, 600-2048 tokens per
+    source): the cluster layout, the scatter and the per-token combine."""
+    wl, mode = _draw_large(seed)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE, combine_mode=mode)
+    buf = GH.make_buffer(wl, combine_mode=mode)
+    try:
+        recvs, replies, res = GH.run_exchange(buf, wl, GH.to_device(inp), mode=GH.SCALE)
+        torch.cuda.synchronize()
+        GH.check_layout(wl, GH.snapshot(recvs), exp, False, buf)
+        GH.check_outputs(wl, res, exp)
+    finally:
+        buf.close()
