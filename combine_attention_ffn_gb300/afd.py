@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libafd.so")
 
 OK, ERR_ARG, ERR_STATE, ERR_BUCKET, ERR_RECEIPT = 0, 1, 2, 3, 4
 ERR_ROUTE_RANGE, ERR_ROUTE_DUP, ERR_CUDA, ERR_OOM, ERR_CAPTURING, ERR_UNSUPPORTED = 5, 6, 7, 8, 9, 10
+ERR_TIMEOUT = 11
 BF16, FP8_E4M3 = 0, 1
 COMBINE_FUSED, COMBINE_TWO_STAGE, COMBINE_TWO_STAGE_FP8 = 0, 1, 2
 

@@ -391,6 +391,115 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   fill_padding(p, p.ends);
 }
 
+// ---- bulk-copy scatter (rows of at most kBulkRowMax bytes in device memory)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// One bulk copy of `bytes` from global memory into shared memory, completing
+// on the barrier (which expects that many bytes).
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst_smem)),
+               "l"(src), "r"(bytes), "r"(smem_addr(mbar))
+               : "memory");
+}
+
+// Waits for the barrier's phase `parity` to complete, a bounded number of
+// polls (each poll may suspend the thread for a while); false if it gave up.
+__device__ __forceinline__ bool wait_phase(uint64_t* mbar, uint32_t parity) {
+  for (int i = 0; i < (1 << 22); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(smem_addr(mbar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
+               "r"(bytes)
+               : "memory");
+}
+
+// The scatter with bulk (TMA) copies: a warp per token; lane 0 brings the
+// row into the warp's shared-memory buffer with one bulk copy, and lane k < K
+// writes it to route k's row with one bulk copy, while the lanes write the
+// receipts (and FP8 scales) with ordinary stores. The buffer is reused for
+// the warp's next token once every lane's copies have read it.
+__global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_bulk_kernel(const __grid_constant__ DispatchParams p) {
+  extern __shared__ __align__(128) uint8_t bsm[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(bsm) + wib;       // one barrier per warp
+  uint8_t* buf = bsm + 128 + (size_t)wib * p.row_bytes;          // one row per warp
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K;
+  const uint32_t rb = (uint32_t)p.row_bytes;
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(mbar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  pdl_launch_dependents();
+  // the source rows are inputs, not layout outputs: load the first one while
+  // the layout is still running
+  if (lane == 0 && gwarp < p.total_tokens) {
+    const int s0 = source_of_token(p, gwarp);
+    bulk_load(buf, p.src[s0].x + (int64_t)(gwarp - p.src[s0].tok_off) * rb, rb, mbar);
+  }
+  pdl_wait();  // the layout kernel's route codes
+
+  uint32_t parity = 0;
+  int gt = gwarp;
+  for (; gt < p.total_tokens; gt += nwarps) {
+    const int s = source_of_token(p, gt);
+    const SourceDesc& src = p.src[s];
+    const int t = gt - src.tok_off;
+    if (gt != gwarp && lane == 0) bulk_load(buf, src.x + (int64_t)t * rb, rb, mbar);
+    const int code = lane < K ? __ldcg(p.route_tmp + (int64_t)gt * K + lane) : -1;
+    if (lane < K) {
+      if (code >= 0)
+        write_route(p, s, t, gt, code, src.w[(int64_t)t * K + lane]);
+      else
+        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+    }
+    for (int b0 = 0; b0 < p.nscale; b0 += 32) {  // FP8: the row's block scales follow it
+      const int b = b0 + lane;
+      const float sc = b < p.nscale ? src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb] : 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const int c = __shfl_sync(0xffffffffu, code, k);
+        if (c >= 0 && b < p.nscale)
+          p.row_scales[((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.nscale + b] = sc;
+      }
+    }
+    const bool arrived = wait_phase(mbar, parity);
+    if (!arrived) break;
+    parity ^= 1u;
+    if (code >= 0)
+      bulk_store(p.rows + ((int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)) * rb, buf, rb);
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // this lane's copies have read buf
+    __syncwarp();
+  }
+  if (gt < p.total_tokens) {  // a wait gave up: report it, give the load in flight one more bounded wait
+    if (lane == 0) {
+      const int s = source_of_token(p, gt);
+      atomicMin(p.err, route_error_key(s, gt - p.src[s].tok_off, 0, kErrTimeout));
+    }
+    wait_phase(mbar, parity);
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this lane's copies are complete
+  fill_padding(p, p.ends);
+}
+
 // Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
 // or -1 for none). kPre: `pre` holds the row's first piece.
 template <bool kPre>
@@ -753,7 +862,7 @@ cudaError_t configure_dispatch_kernels(int* max_ctas) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
-  for (const void* k : {(const void*)cluster_layout_kernel, (const void*)scatter_kernel,
+  for (const void* k : {(const void*)cluster_layout_kernel, (const void*)scatter_kernel, (const void*)scatter_bulk_kernel,
                         (const void*)dispatch_small_kernel, (const void*)dispatch_tiny_kernel,
                         (const void*)cached_scatter_kernel})
     if (e == cudaSuccess)
@@ -829,6 +938,9 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
   int grid = (p.total_tokens + kWarps - 1) / kWarps;
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
+  if (p.x_device && p.row_bytes <= kBulkRowMax)
+    return launch(scatter_bulk_kernel, grid, AFD_SCATTER_BLOCK, 128 + (size_t)kWarps * p.row_bytes, stream, true,
+                  p);
   return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
 }
 

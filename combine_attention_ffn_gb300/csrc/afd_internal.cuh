@@ -49,8 +49,10 @@ static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 // its split, which cost up to 6 us per round trip.
 constexpr int kSharedCarveout = 50;  // percent of the maximum shared memory
 
-constexpr int kErrRange = 5;  // AFD_ERR_ROUTE_RANGE
-constexpr int kErrDup = 6;    // AFD_ERR_ROUTE_DUP
+constexpr int kErrRange = 5;    // AFD_ERR_ROUTE_RANGE
+constexpr int kErrDup = 6;      // AFD_ERR_ROUTE_DUP
+constexpr int kErrTimeout = 11; // AFD_ERR_TIMEOUT
+constexpr int kBulkRowMax = 4096;  // rows up to this many bytes take the bulk-copy scatter
 constexpr unsigned long long kNoError = ~0ull;
 
 // The sticky route error: the smallest key wins, so the reported route is the
@@ -68,6 +70,8 @@ struct SourceDesc {
   int64_t sst, ssb;
   int32_t T;             // live tokens
   int32_t tok_off;       // first flattened token of this source
+  int32_t x_device;      // x is device memory (not host memory mapped for the device)
+  int32_t pad_;
 };
 
 // Everything the layout and scatter kernels of one exchange read or write.
@@ -78,6 +82,7 @@ struct DispatchParams {
   int32_t nscale;        // H / 128 for FP8, else 0
   int32_t total_tokens;  // sum of T
   int32_t layout_ctas;   // CTAs of the layout cluster (large path)
+  int32_t x_device;      // 1 when every source's rows are in device memory (bulk copies allowed)
   int64_t R_arena;       // rows per worker arena
   // context scratch
   int32_t* route_tmp;    // [total_tokens][K]: the layout's route codes, (worker << 24) | row, or -1

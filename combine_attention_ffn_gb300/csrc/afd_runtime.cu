@@ -131,8 +131,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // context's device, managed memory, or page-locked host memory (reached over
 // the host link through its mapped device address). Pageable host memory is
 // refused: a kernel cannot dereference it.
-afd_status resolve_ptr(afd_ctx* c, const void* p, const char* what, const void** out) {
+afd_status resolve_ptr(afd_ctx* c, const void* p, const char* what, const void** out,
+                       bool* on_device = nullptr) {
   DeviceGuard guard(c->device);  // a mapped host address is the current device's
+  if (on_device) *on_device = false;
   cudaPointerAttributes a;
   memset(&a, 0, sizeof a);
   cudaError_t e = cudaPointerGetAttributes(&a, p);
@@ -145,6 +147,7 @@ afd_status resolve_ptr(afd_ctx* c, const void* p, const char* what, const void**
       if (a.device != c->device)
         return fail(c, AFD_ERR_ARG, "%s is on device %d, the context on device %d", what, a.device, c->device);
       *out = p;
+      if (on_device) *on_device = true;
       return AFD_OK;
     case cudaMemoryTypeManaged:
       *out = p;
@@ -270,11 +273,13 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   DispatchParams p;
   memset(&p, 0, sizeof p);
   int tok = 0;
+  p.x_device = 1;
   for (int s = 0; s < g.num_sources; ++s) {
     p.src[s] = c->src[s];
     p.src[s].tok_off = tok;
     c->src[s].tok_off = tok;
     tok += c->src[s].T;
+    if (c->src[s].T > 0 && !c->src[s].x_device) p.x_device = 0;
   }
   p.A = g.num_sources;
   p.F = g.num_workers;
@@ -327,6 +332,7 @@ const char* afd_status_string(afd_status s) {
     case AFD_ERR_OOM: return "allocation failed";
     case AFD_ERR_CAPTURING: return "host synchronization requested during stream capture";
     case AFD_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case AFD_ERR_TIMEOUT: return "a bounded device-side wait gave up";
   }
   return "unknown status";
 }
@@ -464,12 +470,13 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
   const int64_t* dids = nullptr;
   const float* dw = nullptr;
   const float* dsc = nullptr;
+  bool x_dev = true;
   if (num_tokens > 0) {
     if (!x || !ids || !weights) return fail(c, AFD_ERR_ARG, "x, ids and weights are required");
     if (g.dtype == AFD_FP8_E4M3 && !x_scale) return fail(c, AFD_ERR_ARG, "FP8 dispatch needs x_scale");
     if (g.dtype == AFD_FP8_E4M3 && (scale_stride_t < 0 || scale_stride_b < 0))
       return fail(c, AFD_ERR_ARG, "scale strides must be non-negative");
-    afd_status r = resolve_ptr(c, x, "x", &dx);
+    afd_status r = resolve_ptr(c, x, "x", &dx, &x_dev);
     if (r == AFD_OK) r = resolve(c, ids, "ids", &dids);
     if (r == AFD_OK) r = resolve(c, weights, "weights", &dw);
     if (r == AFD_OK && g.dtype == AFD_FP8_E4M3) r = resolve(c, x_scale, "x_scale", &dsc);
@@ -486,6 +493,7 @@ afd_status afd_source_dispatch(afd_ctx* c, int32_t source, const void* x, const 
 
   SourceDesc& d = c->src[source];
   d.x = static_cast<const uint8_t*>(dx);
+  d.x_device = x_dev ? 1 : 0;
   d.ids = dids;
   d.w = dw;
   d.scale = dsc;
@@ -528,12 +536,13 @@ afd_status afd_source_dispatch_cached(afd_ctx* c, int32_t source, const void* x,
   const void* dx = nullptr;
   const float* dw = nullptr;
   const float* dsc = nullptr;
+  bool x_dev = true;
   if (num_tokens > 0) {
     if (!x) return fail(c, AFD_ERR_ARG, "x is required");
     if (g.dtype == AFD_FP8_E4M3 && !x_scale) return fail(c, AFD_ERR_ARG, "FP8 dispatch needs x_scale");
     if (g.dtype == AFD_FP8_E4M3 && (scale_stride_t < 0 || scale_stride_b < 0))
       return fail(c, AFD_ERR_ARG, "scale strides must be non-negative");
-    afd_status r = resolve_ptr(c, x, "x", &dx);
+    afd_status r = resolve_ptr(c, x, "x", &dx, &x_dev);
     if (r == AFD_OK && weights) r = resolve(c, weights, "weights", &dw);
     if (r == AFD_OK && g.dtype == AFD_FP8_E4M3) r = resolve(c, x_scale, "x_scale", &dsc);
     if (r != AFD_OK) return r;
@@ -548,6 +557,7 @@ afd_status afd_source_dispatch_cached(afd_ctx* c, int32_t source, const void* x,
 
   SourceDesc& d = c->src[source];
   d.x = static_cast<const uint8_t*>(dx);
+  d.x_device = x_dev ? 1 : 0;
   d.ids = nullptr;
   d.w = dw;
   d.scale = dsc;

@@ -77,7 +77,9 @@ typedef enum afd_status {
   AFD_ERR_CUDA = 7,         /* a CUDA runtime call failed (see afd_error_detail) */
   AFD_ERR_OOM = 8,          /* device or pinned allocation failed at create */
   AFD_ERR_CAPTURING = 9,    /* a host-synchronizing request on a capturing stream */
-  AFD_ERR_UNSUPPORTED = 10  /* configuration outside what this build implements */
+  AFD_ERR_UNSUPPORTED = 10, /* configuration outside what this build implements */
+  AFD_ERR_TIMEOUT = 11      /* a bounded device-side wait gave up (reported like a route
+                               error, through afd_get_error; the outputs are unspecified) */
 } afd_status;
 
 enum { AFD_BF16 = 0, AFD_FP8_E4M3 = 1 };
@@ -266,12 +268,13 @@ AFD_API afd_status afd_source_collect(afd_ctx* ctx, int32_t source, void* out, i
 AFD_API afd_status afd_source_collect_all(afd_ctx* ctx, void* const* outs, int32_t view,
                                           afd_stream stream, afd_view* views);
 
-/* The sticky route error found on the GPU. Synchronizes the context's device
- * work first. code = AFD_OK, AFD_ERR_ROUTE_RANGE or AFD_ERR_ROUTE_DUP; for an
- * error, (source, token, k) is the invalid route that comes first in
- * (source, token, k) order among all exchanges since the last
- * afd_clear_error. Any pointer may be NULL. Not allowed while the context's
- * last stream is capturing (AFD_ERR_CAPTURING). */
+/* The sticky error found on the GPU. Synchronizes the context's device work
+ * first. code = AFD_OK, AFD_ERR_ROUTE_RANGE or AFD_ERR_ROUTE_DUP (for these,
+ * (source, token, k) is the invalid route that comes first in (source,
+ * token, k) order among all exchanges since the last afd_clear_error), or
+ * AFD_ERR_TIMEOUT (a bounded wait of the scatter's bulk copies gave up at
+ * (source, token); k = 0). Any pointer may be NULL. Not allowed while the
+ * context's last stream is capturing (AFD_ERR_CAPTURING). */
 AFD_API afd_status afd_get_error(afd_ctx* ctx, int32_t* code, int32_t* source, int32_t* token,
                          int32_t* k);
 

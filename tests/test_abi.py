@@ -55,6 +55,9 @@ def test_status_strings_and_no_device(lib_path):
     lib = afd.load_library(lib_path)
     assert lib.afd_status_string(0) == b"ok"
     assert b"receipt" in lib.afd_status_string(afd.ERR_RECEIPT)
+    assert b"wait" in lib.afd_status_string(afd.ERR_TIMEOUT)
+    for code in range(12):  # every status has its own text
+        assert lib.afd_status_string(code) != lib.afd_status_string(99)
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; the no-device path is not reachable")
     cfg = afd.Config(2, 2, 8, 2, 256, 16, 1, 0, 0)
