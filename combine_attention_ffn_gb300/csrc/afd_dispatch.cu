@@ -434,7 +434,7 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
 // writes it to route k's row with one bulk copy, while the lanes write the
 // receipts (and FP8 scales) with ordinary stores. The buffer is reused for
 // the warp's next token once every lane's copies have read it.
-__global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_bulk_kernel(const __grid_constant__ DispatchParams p) {
+__global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(128) uint8_t bsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(bsm) + wib;       // one barrier per warp
@@ -938,9 +938,14 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
   int grid = (p.total_tokens + kWarps - 1) / kWarps;
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
   if (grid < 1) grid = 1;
-  if (p.x_device && p.row_bytes <= kBulkRowMax)
-    return launch(scatter_bulk_kernel, grid, AFD_SCATTER_BLOCK, 128 + (size_t)kWarps * p.row_bytes, stream, true,
-                  p);
+  if (p.x_device && p.row_bytes <= kBulkRowMax) {
+    // two-warp blocks: a row buffer per warp, so that blocks stay small and many
+    constexpr int kBulkWarps = 2;
+    int bgrid = (p.total_tokens + kBulkWarps - 1) / kBulkWarps;
+    if (bgrid > sm_cap * 32) bgrid = sm_cap * 32;
+    return launch(scatter_bulk_kernel, bgrid, 32 * kBulkWarps, 128 + (size_t)kBulkWarps * p.row_bytes, stream,
+                  true, p);
+  }
   return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
 }
 

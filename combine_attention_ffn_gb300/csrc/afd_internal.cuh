@@ -52,7 +52,7 @@ constexpr int kSharedCarveout = 50;  // percent of the maximum shared memory
 constexpr int kErrRange = 5;    // AFD_ERR_ROUTE_RANGE
 constexpr int kErrDup = 6;      // AFD_ERR_ROUTE_DUP
 constexpr int kErrTimeout = 11; // AFD_ERR_TIMEOUT
-constexpr int kBulkRowMax = 4096;  // rows up to this many bytes take the bulk-copy scatter
+constexpr int kBulkRowMax = 8192;  // rows up to this many bytes take the bulk-copy scatter
 constexpr unsigned long long kNoError = ~0ull;
 
 // The sticky route error: the smallest key wins, so the reported route is the
