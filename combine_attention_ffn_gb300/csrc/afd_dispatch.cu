@@ -434,6 +434,10 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
 // writes it to route k's row with one bulk copy, while the lanes write the
 // receipts (and FP8 scales) with ordinary stores. The buffer is reused for
 // the warp's next token once every lane's copies have read it.
+// kCached: the copy along the last exchange's receipts (cached dispatch):
+// the route codes come from the receipt, and new weights, when given,
+// replace the old ones in both receipts.
+template <bool kCached>
 __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(128) uint8_t bsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
@@ -448,14 +452,19 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  pdl_launch_dependents();
+  if (kCached) {  // the first kernel of the exchange (see cluster_layout_kernel)
+    pdl_wait();
+    pdl_launch_dependents();
+  } else {
+    pdl_launch_dependents();
+  }
   // the source rows are inputs, not layout outputs: load the first one while
   // the layout is still running
   if (lane == 0 && gwarp < p.total_tokens) {
     const int s0 = source_of_token(p, gwarp);
     bulk_load(buf, p.src[s0].x + (int64_t)(gwarp - p.src[s0].tok_off) * rb, rb, mbar);
   }
-  pdl_wait();  // the layout kernel's route codes
+  if (!kCached) pdl_wait();  // the layout kernel's route codes
 
   uint32_t parity = 0;
   int gt = gwarp;
@@ -464,12 +473,25 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
     const SourceDesc& src = p.src[s];
     const int t = gt - src.tok_off;
     if (gt != gwarp && lane == 0) bulk_load(buf, src.x + (int64_t)t * rb, rb, mbar);
-    const int code = lane < K ? __ldcg(p.route_tmp + (int64_t)gt * K + lane) : -1;
-    if (lane < K) {
-      if (code >= 0)
-        write_route(p, s, t, gt, code, src.w[(int64_t)t * K + lane]);
-      else
-        p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+    int code = -1;
+    if (kCached) {
+      if (lane < K) {
+        int2* r = p.routes + (int64_t)gt * K + lane;
+        code = r->x;
+        if (src.w != nullptr && code >= 0) {
+          const float w = src.w[(int64_t)t * K + lane];
+          r->y = __float_as_int(w);
+          p.row_w[(int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)] = w;
+        }
+      }
+    } else {
+      code = lane < K ? __ldcg(p.route_tmp + (int64_t)gt * K + lane) : -1;
+      if (lane < K) {
+        if (code >= 0)
+          write_route(p, s, t, gt, code, src.w[(int64_t)t * K + lane]);
+        else
+          p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
+      }
     }
     for (int b0 = 0; b0 < p.nscale; b0 += 32) {  // FP8: the row's block scales follow it
       const int b = b0 + lane;
@@ -497,7 +519,7 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
     wait_phase(mbar, parity);
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this lane's copies are complete
-  fill_padding(p, p.ends);
+  if (!kCached) fill_padding(p, p.ends);
 }
 
 // Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
@@ -862,7 +884,8 @@ cudaError_t configure_dispatch_kernels(int* max_ctas) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmallSmemMax);
-  for (const void* k : {(const void*)cluster_layout_kernel, (const void*)scatter_kernel, (const void*)scatter_bulk_kernel,
+  for (const void* k : {(const void*)cluster_layout_kernel, (const void*)scatter_kernel,
+                        (const void*)scatter_bulk_kernel<false>, (const void*)scatter_bulk_kernel<true>,
                         (const void*)dispatch_small_kernel, (const void*)dispatch_tiny_kernel,
                         (const void*)cached_scatter_kernel})
     if (e == cudaSuccess)
@@ -943,8 +966,8 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
     constexpr int kBulkWarps = 2;
     int bgrid = (p.total_tokens + kBulkWarps - 1) / kBulkWarps;
     if (bgrid > sm_cap * 32) bgrid = sm_cap * 32;
-    return launch(scatter_bulk_kernel, bgrid, 32 * kBulkWarps, 128 + (size_t)kBulkWarps * p.row_bytes, stream,
-                  true, p);
+    return launch(scatter_bulk_kernel<false>, bgrid, 32 * kBulkWarps, 128 + (size_t)kBulkWarps * p.row_bytes,
+                  stream, true, p);
   }
   return launch(scatter_kernel, grid, AFD_SCATTER_BLOCK, 0, stream, true, p);
 }
@@ -956,6 +979,14 @@ namespace afd {
 // A programmatic dependent of the work before it, which it waits for before
 // it rewrites the rows that the previous exchange's combine reads.
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
+  if (p.x_device && p.row_bytes <= kBulkRowMax) {
+    constexpr int kBulkWarps = 2;
+    int bgrid = (p.total_tokens + kBulkWarps - 1) / kBulkWarps;
+    if (bgrid > sm_cap * 32) bgrid = sm_cap * 32;
+    if (bgrid < 1) bgrid = 1;
+    return launch(scatter_bulk_kernel<true>, bgrid, 32 * kBulkWarps, 128 + (size_t)kBulkWarps * p.row_bytes,
+                  stream, true, p);
+  }
   constexpr int kWarps = AFD_SCATTER_BLOCK / 32;
   int grid = (p.total_tokens + kWarps - 1) / kWarps;
   if (grid > sm_cap * (2048 / AFD_SCATTER_BLOCK)) grid = sm_cap * (2048 / AFD_SCATTER_BLOCK);
