@@ -48,13 +48,20 @@ __device__ __forceinline__ int source_of_token(const DispatchParams& p, int gt) 
 // ones in its warp's lane masks (wmask = this warp's [E] masks). Returns the
 // set of valid routes (bit k). IDs are read as int64 so that a value outside
 // int32 is out of range, not truncated. Errors go to `err` when it is given.
+// The experts of routes 0..7 stay in e8 (registers), so that the caller can
+// rank them without reading the IDs again (meaningful for valid routes only).
 __device__ __forceinline__ uint32_t mark_token(const int64_t* ids, int K, int E, uint32_t* wmask,
-                                               int lane, int s, int t, unsigned long long* err) {
+                                               int lane, int s, int t, unsigned long long* err,
+                                               int (&e8)[8]) {
   uint32_t valid = 0u;
   for (int k0 = 0; k0 < K; k0 += 8) {
     int64_t v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = (k0 + j < K) ? ids[k0 + j] : -1;
+    if (k0 == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e8[j] = (int)v[j];
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int k = k0 + j;
@@ -267,7 +274,7 @@ __device__ __forceinline__ int layout_tpc(const DispatchParams& p) {
   return (p.total_tokens + p.layout_ctas - 1) / p.layout_ctas;
 }
 
-__global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_constant__ DispatchParams p) {
+__global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_constant__ DispatchParams p) {
   extern __shared__ __align__(16) uint32_t smem[];
   const int E = p.E, K = p.K, N = p.total_tokens;
   uint32_t* mask = smem;                                        // [8][E]
@@ -308,7 +315,8 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
     for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) mask[i] = 0u;
     __syncthreads();
     const int64_t* ids = p.src[s].ids + (int64_t)t * K;
-    const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err) : 0u;
+    int e8[8];
+    const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err, e8) : 0u;
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       int run = cnt[e];
@@ -322,7 +330,17 @@ __global__ void __launch_bounds__(kChunk) cluster_layout_kernel(const __grid_con
     __syncthreads();
     if (live) {
       int32_t* mine = codes + (int64_t)(gt - lo) * K;
-      for (int k = 0; k < K; ++k) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k >= K) continue;
+        int code = -1;
+        if ((valid >> k) & 1u) {
+          const int e = e8[k];
+          code = (e << kLocalRankBits) | (wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before));
+        }
+        mine[k] = code;
+      }
+      for (int k = 8; k < K; ++k) {
         int code = -1;
         if ((valid >> k) & 1u) {
           const int e = (int)ids[k];
@@ -591,11 +609,12 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
     int s = 0, t = 0;
     const int64_t* ids = nullptr;
     uint32_t valid = 0u;
+    int e8[8];
     if (live) {
       s = source_of_token(p, gt);
       t = gt - p.src[s].tok_off;
       ids = p.src[s].ids + (int64_t)t * K;
-      valid = mark_token(ids, K, E, mask + warp * E, lane, s, t, err);
+      valid = mark_token(ids, K, E, mask + warp * E, lane, s, t, err, e8);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -610,7 +629,18 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
     __syncthreads();
     if (live) {
       const uint32_t lanes_before = (1u << lane) - 1u;
-      for (int k = 0; k < K; ++k) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k >= K) continue;
+        uint32_t info = ~0u;
+        if ((valid >> k) & 1u) {
+          const int e = e8[k];
+          info = ((uint32_t)e << kRankBits) |
+                 (uint32_t)(wbase[warp * E + e] + __popc(mask[warp * E + e] & lanes_before));
+        }
+        rinfo[gt * K + k] = info;
+      }
+      for (int k = 8; k < K; ++k) {
         uint32_t info = ~0u;
         if ((valid >> k) & 1u) {
           const int e = (int)ids[k];
@@ -795,8 +825,9 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   if (lane < N) {
     const int ls = source_of_token(p, lane);
     const int lt = lane - p.src[ls].tok_off;
+    int e8[8];
     valid = mark_token(p.src[ls].ids + (int64_t)lt * K, K, E, mask, lane, ls, lt,
-                       blockIdx.x == 0 ? p.err : nullptr);
+                       blockIdx.x == 0 ? p.err : nullptr, e8);
   }
   __syncwarp();
   warp_worker_scan(p, [&](int e) { return __popc(mask[e]); }, sh_start, sh_end, blockIdx.x == 0);
