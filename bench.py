@@ -694,7 +694,9 @@ def main():
     # dominant kernel: the combine has the largest share of the launch list
     # (profiles/launches_*.md); one launch per source for F > 1, one for all
     # sources for F = 1. The dispatch phase (layout + scatter) is reported too.
-    comb_ms = r_ms + c_ms  # F = 1 combines at reply, F > 1 at collect
+    # F = 1 combines at reply (its collect is a view or a copy); F > 1 combines
+    # at collect, and its receive/reply graph launches no kernel at all
+    comb_ms = r_ms if wl.F == 1 else c_ms
     n_launch = wl.A if wl.F > 1 else 1
     per_launch_s = comb_ms / n_launch * 1e-3
     per_launch_bytes = ab["combine"] / n_launch
