@@ -37,6 +37,9 @@ namespace {
 
 constexpr int kGroup = 8;  // routes whose loads are issued together
 
+// Resident blocks per SM of combine_kernel<1> (set by configure_combine_kernels).
+int g_seg1_blocks_per_sm = 0;
+
 __device__ __forceinline__ int source_of(const CombineParams& p, int gt) {
   int s = 0;
   while (s + 1 < p.A && gt >= p.tok_off[s + 1]) ++s;
@@ -376,8 +379,11 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
   }
   const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
   const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
-  // Two slices per item once there is enough work to fill the device twice.
-  const bool wide = (p.H % 512 == 0) && slices >= 2 * cap * 8;
+  // Two slices per item when one slice per warp would need more warps than
+  // the SMs hold at once: every warp then still has exactly one item, in a
+  // single wave, instead of a second wave paying the whole latency again.
+  const int64_t resident1 = (int64_t)sm_cap * (g_seg1_blocks_per_sm > 0 ? g_seg1_blocks_per_sm : 1) * 8;
+  const bool wide = (p.H % 512 == 0) && slices > resident1;
   const int64_t items = wide ? slices / 2 : slices;
   int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;
@@ -396,6 +402,7 @@ cudaError_t configure_combine_kernels() {
                         (const void*)copy_kernel})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg1_blocks_per_sm, combine_kernel<1>, 256, 0);
   return e;
 }
 
