@@ -589,15 +589,21 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
 
-  // Load this warp's first (token, route) pair's row and weight now, so that
-  // their latency overlaps the counting below.
-  uint4 pre[kScatterVecs];
-  float pre_w = 0.0f;
-  const bool have_pre = gwarp < N * K;
-  if (have_pre) {
+  // Load this warp's first two (token, route) pairs' rows and weights now,
+  // so that their latency overlaps the counting below (a launch has at most
+  // two pairs per warp up to kSmallRoutes routes on a full device).
+  uint4 pre[kScatterVecs], pre2[kScatterVecs];
+  float pre_w = 0.0f, pre2_w = 0.0f;
+  if (gwarp < N * K) {
     const int gt = gwarp / K, s = source_of_token(p, gt), t = gt - p.src[s].tok_off;
     load_piece(pre, reinterpret_cast<const uint4*>(p.src[s].x + (int64_t)t * p.row_bytes), 0, p.row_bytes >> 4);
     if (lane == 0) pre_w = p.src[s].w[(int64_t)t * K + (gwarp - gt * K)];
+  }
+  if (gwarp + nwarps < N * K) {
+    const int pr = gwarp + nwarps;
+    const int gt = pr / K, s = source_of_token(p, gt), t = gt - p.src[s].tok_off;
+    load_piece(pre2, reinterpret_cast<const uint4*>(p.src[s].x + (int64_t)t * p.row_bytes), 0, p.row_bytes >> 4);
+    if (lane == 0) pre2_w = p.src[s].w[(int64_t)t * K + (pr - gt * K)];
   }
 
   // Pass 1 (every block, all routes): ranks inside each chunk, chunk counts.
@@ -676,7 +682,7 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
     int code = -1;
     if (lane == 0) {
       const uint32_t info = rinfo[gt * K + kk];
-      const float w = pr == gwarp ? pre_w : src.w[(int64_t)t * K + kk];
+      const float w = pr == gwarp ? pre_w : pr == gwarp + nwarps ? pre2_w : src.w[(int64_t)t * K + kk];
       if (info != ~0u) {
         const int e = (int)(info >> kRankBits);
         const int row = sh_start[e] + ccnt[(gt / kChunk) * E + e] + (int)(info & ((1u << kRankBits) - 1));
@@ -693,6 +699,8 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
     code = __shfl_sync(0xffffffffu, code, 0);
     if (pr == gwarp)
       copy_route<true>(p, src, t, code, pre);
+    else if (pr == gwarp + nwarps)
+      copy_route<true>(p, src, t, code, pre2);
     else
       copy_route<false>(p, src, t, code, pre);
   }
