@@ -188,6 +188,30 @@ afd_status scratch_for_current_device(int32_t** out) {
   return AFD_OK;
 }
 
+// The address a kernel on the current device uses for a caller buffer: the
+// buffer itself in that device's memory or in managed memory, the mapped
+// device address of page-locked host memory. Pageable host memory, and
+// memory of another device, are refused before anything is enqueued.
+template <typename T>
+bool device_view(T* p, T** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaPointerAttributes a = {};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if ((a.type == cudaMemoryTypeDevice && a.device == dev) || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *out = static_cast<T*>(a.devicePointer);
+    return true;
+  }
+  return false;
+}
+
 }  // namespace
 
 extern "C" AFD_API afd_status afd_route_layout_noalloc(const int64_t* ids, int32_t num_tokens,
@@ -201,6 +225,9 @@ extern "C" AFD_API afd_status afd_route_layout_noalloc(const int64_t* ids, int32
     return AFD_ERR_ARG;
   if (T > kNaMaxTokens || K > kNaMaxTopK || E > kNaMaxExperts || (int64_t)T * K > kNaMaxRoutes)
     return AFD_ERR_UNSUPPORTED;
+  if ((T > 0 && (!device_view(ids, &ids) || !device_view(slots, &slots))) || !device_view(ends, &ends) ||
+      !device_view(error, &error))
+    return AFD_ERR_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int32_t* scratch = nullptr;
   afd_status st = scratch_for_current_device(&scratch);

@@ -317,6 +317,9 @@ AFD_API int64_t afd_recv_rows_for_bucket(const afd_ctx* ctx, int32_t bucket);
  *              AFD_ERR_ROUTE_DUP), or {AFD_OK, -1, -1}
  * Limits: num_tokens <= 8192, top_k <= 32, num_tokens * top_k <= 65536,
  * num_experts <= 1024; larger sizes return AFD_ERR_UNSUPPORTED and enqueue
+ * nothing. Every buffer must be reachable from the current device (its
+ * device memory, managed memory, or page-locked host memory); pageable host
+ * memory or another device's memory returns AFD_ERR_ARG and enqueues
  * nothing. Work is enqueued on `stream` (the current device's).
  * The first call on a device looks up the scratch array's device address
  * (and sets a kernel attribute); make that first call before any stream

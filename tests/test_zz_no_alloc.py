@@ -110,3 +110,24 @@ def test_noalloc_reports_invalid_route_and_rejects_oversize():
                                       ctypes.c_void_p(1), ctypes.c_void_p(1), ctypes.c_void_p(1),
                                       None)
     assert st == afd.ERR_UNSUPPORTED
+
+
+def test_noalloc_refuses_pageable_host_buffers():
+    """Buffers the GPU cannot reach (pageable host memory) are refused on the
+    host, before anything is enqueued."""
+    lib = afd.load_library()
+    ids_dev = torch.zeros((4, 2), dtype=torch.int64, device="cuda")
+    ids_dev[:, 1] = 1
+    ends_host = np.zeros(8, dtype=np.int32)            # pageable
+    slots = torch.zeros((4, 2), dtype=torch.int32, device="cuda")
+    err = torch.zeros((3,), dtype=torch.int32, device="cuda")
+    st = lib.afd_route_layout_noalloc(
+        ctypes.c_void_p(ids_dev.data_ptr()), 4, 2, 8, 2, 1, ctypes.c_void_p(ends_host.ctypes.data),
+        ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(err.data_ptr()), None)
+    assert st == afd.ERR_ARG
+    ids_host = ids_dev.cpu().numpy()                   # pageable
+    ends = torch.zeros((8,), dtype=torch.int32, device="cuda")
+    st = lib.afd_route_layout_noalloc(
+        ctypes.c_void_p(ids_host.ctypes.data), 4, 2, 8, 2, 1, ctypes.c_void_p(ends.data_ptr()),
+        ctypes.c_void_p(slots.data_ptr()), ctypes.c_void_p(err.data_ptr()), None)
+    assert st == afd.ERR_ARG
