@@ -29,6 +29,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "dispatch+combine µs/round trip; achieved HBM GB/s vs peak (E128 K8 H2048)"
+COMBINE_MODES = {"fused": 0, "two-stage": 1, "two-stage-fp8": 2}  # afd_config.combine_mode
 FALLBACK_HBM_GBS = 6800.0
 PAGES_CONTEXT_US = {  # afdEP-comm design page, "Result" table: 4 x H100 NVLink, communication only
     ("2A2F", 2048, 1): 20.7, ("2A2F", 2048, 2048): 192.7,
@@ -43,6 +44,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="2A2F")
+    ap.add_argument("--combine-mode", choices=list(COMBINE_MODES), default="fused",
+                    help="fused: one FP32 sum over every route, one rounding; two-stage: BF16 "
+                         "partial per worker, then their FP32 sum; two-stage-fp8: the partials as "
+                         "E4M3 with one power-of-two scale per 128 values")
     ap.add_argument("--tokens", type=int, default=2048, help="tokens per source")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -221,7 +226,7 @@ def dist_env():
 
 
 # ------------------------------------------------------------------ reference arm
-def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1):
+def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1, combine_mode: str = "fused"):
     """Times the oracle's dispatch + combine (identity expert) on this host."""
     import oracle
 
@@ -236,7 +241,11 @@ def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1):
         r_stride = max(1, int(lay["r_exact"].max()))
         d = oracle.dispatch(p, inp.ids, inp.w, inp.x, inp.x_scales, lay, r_stride)
         reply = d["rows"].view(np.uint16).reshape(wl.F, r_stride, wl.H)
-        oracle.combine(p, inp.ids, inp.w, d["slot"], r_stride, reply)
+        if combine_mode == "fused":
+            oracle.combine(p, inp.ids, inp.w, d["slot"], r_stride, reply)
+        else:
+            oracle.combine_two_stage(p, inp.ids, inp.w, d["slot"], r_stride, reply,
+                                     fp8=combine_mode == "two-stage-fp8")
         times.append((time.perf_counter() - t0) * 1e6)
     return times
 
@@ -252,8 +261,8 @@ def run_reference(args):
     if wl.dtype == "fp8":
         print(json.dumps({"impl": "reference", "unavailable": "the CPU arm times BF16 workloads only"}))
         return 0
-    cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.warmup)  # warm-up
-    steps = cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.steps)
+    cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.warmup, combine_mode=args.combine_mode)  # warm-up
+    steps = cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.steps, combine_mode=args.combine_mode)
     value = statistics.mean(steps)
     ab = algorithmic_bytes(wl, inp)
     line = {
@@ -262,7 +271,7 @@ def run_reference(args):
         "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": workload_config(wl, execution="CPU oracle (single-threaded C) on the host",
-                                  l2="not applicable"),
+                                  l2="not applicable", combine=args.combine_mode),
         "gbs": round(ab["total"] / (value * 1e-6) / 1e9, 2),
         "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle",
@@ -276,13 +285,14 @@ def run_reference(args):
 
 def workload_config(wl, execution: str = "one CUDA graph per round trip",
                     l2: str = "flushed before every timed step (256 MB write, then 256 MB read so the "
-                              "write-backs finish first; outside the step's events)") -> dict:
+                              "write-backs finish first; outside the step's events)",
+                    combine: str = "fused") -> dict:
     return {"workload": f"{wl.name}: A={wl.A} sources x T={wl.T[0]} tokens, F={wl.F} workers, "
                         f"E={wl.E}, K={wl.K}, H={wl.H}, {wl.dtype}, alpha={wl.alpha}, "
                         f"bucket={wl.bucket}, {wl.routing} routing",
             "A": wl.A, "F": wl.F, "E": wl.E, "K": wl.K, "H": wl.H, "T_per_source": wl.T[0],
             "bucket": wl.bucket, "expert_alignment": wl.alpha, "routing": wl.routing,
-            "expert": "identity (reply = received rows)",
+            "expert": "identity (reply = received rows)", "combine": combine,
             "l2": l2, "execution": execution}
 
 
@@ -388,10 +398,12 @@ def run_under_load(args):
     return 0
 
 
-ALL_CONFIGS = (("tiny", (16,)), ("2A2F", (1, 8, 32, 128, 512, 2048)),
-               ("2A2F-H4096", (1, 128, 2048)), ("skew-3A1F", (1, 32, 512, 2048)),
-               ("skew-1A3F", (1, 32, 512, 2048)), ("fp8-2A2F", (1, 128, 2048)),
-               ("fp8-2A1F", (1, 128, 2048)))
+ALL_CONFIGS = (("tiny", (16,), "fused"), ("2A2F", (1, 8, 32, 128, 512, 2048), "fused"),
+               ("2A2F-H4096", (1, 128, 2048), "fused"), ("skew-3A1F", (1, 32, 512, 2048), "fused"),
+               ("skew-1A3F", (1, 32, 512, 2048), "fused"), ("fp8-2A2F", (1, 128, 2048), "fused"),
+               ("fp8-2A1F", (1, 128, 2048), "fused"),
+               # the pages' per-worker rounding (two-stage combine), BF16 and E4M3 partials
+               ("2A2F", (1, 128, 512, 2048), "two-stage"), ("2A2F", (1, 128, 512, 2048), "two-stage-fp8"))
 
 
 def run_all_configs(args):
@@ -425,11 +437,12 @@ def run_all_configs(args):
         return statistics.median(times)
 
     rows = []
-    for name, Ts in ALL_CONFIGS:
+    for name, Ts, mode in ALL_CONFIGS:
         for T in Ts:
             wl = W.named(name, T=T)
             inp = W.make_inputs(wl)
-            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
+            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
+                             combine_mode=COMBINE_MODES[mode])
             fp8 = wl.dtype == "fp8"
             if fp8:
                 xs = [torch.from_numpy(inp.x[s, :t].copy()).to(dev).view(torch.float8_e4m3fn)
@@ -474,7 +487,8 @@ def run_all_configs(args):
                 us = timed_exchange(fp8, first_half, expert, second_half, timed, torch)
                 ab = algorithmic_bytes(wl, inp, view=use_view[0])
                 gbs = ab["total"] / (us * 1e-6) / 1e9
-                rows.append({"config": name + (" view" if use_view[0] else ""), "T": T,
+                rows.append({"config": name + (" view" if use_view[0] else "")
+                             + ("" if mode == "fused" else f" {mode}"), "T": T,
                              "us": round(us, 2), "gbs": round(gbs, 1),
                              "frac": round(gbs / peak, 4) if T >= 512 else None})
             buf.close()
@@ -548,7 +562,8 @@ def main():
     if wl.dtype == "fp8":
         raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
     inp = W.make_inputs(wl)
-    buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype)
+    buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
+                     combine_mode=COMBINE_MODES[args.combine_mode])
     buf_small = sum(wl.T) * wl.K <= 2048 or sum(wl.T) <= 32  # one-kernel dispatch (afd_dispatch.cu)
 
     xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
@@ -700,9 +715,12 @@ def main():
     n_launch = wl.A if wl.F > 1 else 1
     per_launch_s = comb_ms / n_launch * 1e-3
     per_launch_bytes = ab["combine"] / n_launch
-    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * 152 else "combine_kernel"
+    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * 152 else (
+        "combine_kernel" if args.combine_mode == "fused" else "combine_two_stage_kernel")
+    if args.combine_mode != "fused":
+        kname += f" ({args.combine_mode})"
     achieved = per_launch_bytes / per_launch_s / 1e9
-    traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}")
+    traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}") if args.combine_mode == "fused" else None
     d_gbs = ab["dispatch"] / (d_ms * 1e-3) / 1e9
     roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -729,7 +747,7 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and ws == 1:  # the oracle runs at N = 1 only
-        times = cpu_oracle_round_trip_us(wl, inp, args.cpu_seconds)
+        times = cpu_oracle_round_trip_us(wl, inp, args.cpu_seconds, combine_mode=args.combine_mode)
         cpu = {"value": round(statistics.median(times), 1), "unit": "us", "cores": 1, "kind": "oracle",
                "sample": f"{len(times)} full round trips of the same workload "
                          f"(validate, layout, dispatch, combine; identity expert), single-threaded C",
@@ -742,7 +760,7 @@ def main():
             "metric": METRIC, "value": round(us, 2), "unit": "us", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": wl.dtype, "data": "synthetic", "config": workload_config(wl),
+            "dtype": wl.dtype, "data": "synthetic", "config": workload_config(wl, combine=args.combine_mode),
             "gbs": round(ab["total"] / (us * 1e-6) / 1e9, 1),
             "hbm_frac_of_peak": round(ab["total"] / (us * 1e-6) / 1e9 / peak, 4),
             "peak_gbs": peak, "peak_kind": peak_kind,
