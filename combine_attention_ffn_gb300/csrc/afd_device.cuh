@@ -25,7 +25,11 @@ __device__ __forceinline__ uint4 ld_once(const uint4* p) {
   return v;
 }
 
-__device__ __forceinline__ int align_up_dev(int v, int a) { return (v + a - 1) / a * a; }
+// Rounds v up to a multiple of a (a >= 1); a power of two (the usual
+// expert_alignment) takes a mask instead of a division.
+__device__ __forceinline__ int align_up_dev(int v, int a) {
+  return (a & (a - 1)) == 0 ? (v + a - 1) & -a : (v + a - 1) / a * a;
+}
 
 __device__ __forceinline__ int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & 31;
