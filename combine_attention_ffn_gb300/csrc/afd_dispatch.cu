@@ -860,15 +860,28 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
     }
     copy_route<true>(p, src, t, __shfl_sync(0xffffffffu, code, 0), pre);
   }
-  // padding rows, spread over the blocks
+  // padding rows, spread over the blocks: block b takes the experts
+  // b, b + gridDim.x, ...; its lanes look at 32 of them at once, then the
+  // warp writes the padding rows of each one that has some
   if (p.alpha > 1) {
-    for (int e = blockIdx.x; e < E; e += gridDim.x) {
-      const int end = sh_end[e];
-      const int lim = align_up_dev(end, p.alpha);
-      const int64_t base = (int64_t)(e / p.Ef) * p.R_arena;
-      for (int row = end + lane; row < lim; row += 32) {
-        p.row_src[base + row] = -1;
-        p.row_w[base + row] = 0.0f;
+    for (int i0 = 0; (int)blockIdx.x + i0 * (int)gridDim.x < E; i0 += 32) {
+      const int e = (int)blockIdx.x + (i0 + lane) * (int)gridDim.x;
+      int end = 0, lim = 0;
+      if (e < E) {
+        end = sh_end[e];
+        lim = align_up_dev(end, p.alpha);
+      }
+      uint32_t todo = __ballot_sync(0xffffffffu, lim > end);
+      while (todo) {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int pe = __shfl_sync(0xffffffffu, end, src), pl = __shfl_sync(0xffffffffu, lim, src);
+        const int ee = (int)blockIdx.x + (i0 + src) * (int)gridDim.x;
+        const int64_t base = (int64_t)(ee / p.Ef) * p.R_arena;
+        for (int row = pe + lane; row < pl; row += 32) {
+          p.row_src[base + row] = -1;
+          p.row_w[base + row] = 0.0f;
+        }
       }
     }
   }
