@@ -74,3 +74,16 @@ def test_algorithmic_bytes_match_the_formula():
     # payload: read x, write the routed rows, read the replies, write out
     assert ab["payload"] == 2 * 2048 * 4096 + V * 4096 + V * 4096 + 2 * 2048 * 4096
     assert ab["payload"] == 147456 * 2048
+
+
+@pytest.mark.parametrize("mode", ["fused", "two-stage", "two-stage-fp8"])
+def test_reference_arm_reports_the_combine_mode(mode):
+    import json
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--tokens", "16", "--steps", "1", "--warmup", "1",
+                        "--combine-mode", mode], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"]["combine"] == mode
+    assert line["value"] > 0 and line["cpu_baseline"]["cores"] == 1
