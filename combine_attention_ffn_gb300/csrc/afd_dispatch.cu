@@ -794,7 +794,8 @@ __device__ __forceinline__ void warp_worker_scan(const DispatchParams& p, CountO
 }
 
 // At most 32 tokens in the whole exchange: one-warp blocks, one per (token,
-// route) pair (and at least 16, which share the padding rows). Every block
+// route) pair (and at least one per expert up to 128; they share the padding
+// rows). Every block
 // counts all the routes itself with one lane mask per expert (lane = token),
 // so ranks are popcounts of earlier lanes and no block waits for another;
 // block b then writes the receipt of route b % K of token b / K and copies
@@ -978,9 +979,13 @@ cudaError_t configure_dispatch_kernels(int* max_ctas) {
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream) {
   const int block = 256;
   if (p.total_tokens >= 1 && p.total_tokens <= 32 && AFD_TINY_DISPATCH) {
-    // one block per (token, route), and at least 16 blocks to share the padding rows
+    // one block per (token, route), and at least one per expert (up to 128)
+    // so that each block has the padding rows of one expert at most: with 16
+    // blocks for 128 experts the round trip at one token per source took 2 us
+    // longer
     const int pairs = p.total_tokens * p.K;
-    const int grid = pairs > 16 ? pairs : 16;
+    const int min_blocks = p.E < AFD_TINY_MIN_BLOCKS ? p.E : AFD_TINY_MIN_BLOCKS;
+    const int grid = pairs > min_blocks ? pairs : min_blocks;
     return launch(dispatch_tiny_kernel, grid, 32, (size_t)3 * p.E * sizeof(int32_t), stream, true, p);
   }
   if (dispatch_is_small(p)) {

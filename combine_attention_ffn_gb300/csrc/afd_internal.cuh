@@ -27,6 +27,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_SCATTER_BLOCK
 #define AFD_SCATTER_BLOCK 128    // threads per scatter block (a warp per token)
 #endif
+#ifndef AFD_TINY_MIN_BLOCKS
+#define AFD_TINY_MIN_BLOCKS 128   // the one-warp dispatch runs min(E, this) blocks at least (they share the padding rows)
+#endif
 #ifndef AFD_TINY_DISPATCH
 #define AFD_TINY_DISPATCH 1       // exchanges of at most 32 tokens take the one-warp dispatch
 #endif
