@@ -715,7 +715,8 @@ def main():
     n_launch = wl.A if wl.F > 1 else 1
     per_launch_s = comb_ms / n_launch * 1e-3
     per_launch_bytes = ab["combine"] / n_launch
-    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * 152 else (
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * n_sms else (
         "combine_kernel" if args.combine_mode == "fused" else "combine_two_stage_kernel")
     if args.combine_mode != "fused":
         kname += f" ({args.combine_mode})"
