@@ -36,7 +36,8 @@ EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispa
            "afd_worker_reply", "afd_source_collect", "afd_source_collect_all", "afd_get_error",
            "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
-           "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc")
+           "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc",
+           "afd_set_wait_limit")
 
 
 class AfdError(RuntimeError):
@@ -96,6 +97,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_recv_rows_for_bucket": (i64, [v, i32]),
         "afd_version": (i32, []),
         "afd_route_layout_noalloc": (i32, [v, i32, i32, i32, i32, i32, v, v, v, v]),
+        "afd_set_wait_limit": (i32, [v, i32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -357,6 +359,11 @@ class Buffer:
 
     def reset_exchange(self) -> None:
         self._check(self._lib.afd_reset_exchange(self._h), "reset_exchange")
+
+    def set_wait_limit(self, polls: int) -> None:
+        """Polls of each bulk row load before the scatter reports AFD_ERR_TIMEOUT
+        (afd_set_wait_limit; 0 makes every first wait give up at once)."""
+        self._check(self._lib.afd_set_wait_limit(self._h, polls), "set_wait_limit")
 
     def __enter__(self) -> "Buffer":
         return self

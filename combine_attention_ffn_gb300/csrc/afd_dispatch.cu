@@ -426,19 +426,45 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
                : "memory");
 }
 
-// Waits for the barrier's phase `parity` to complete, a bounded number of
-// polls (each poll may suspend the thread for a while); false if it gave up.
-__device__ __forceinline__ bool wait_phase(uint64_t* mbar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(smem_addr(mbar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
+// One poll of the barrier's phase `parity` (the thread may be suspended for a
+// while inside it); true once that phase has completed.
+__device__ __forceinline__ bool phase_done(uint64_t* mbar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(smem_addr(mbar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the barrier's phase `parity`, at most `polls` polls. Every lane
+// polls, and the warp leaves the loop together: once all lanes have seen the
+// phase complete (true), or when the limit is reached (false). A completed
+// phase stays visible until the next arrival, which only lane 0 makes after
+// this wait, so the lanes cannot disagree for long.
+__device__ __forceinline__ bool wait_phase_warp(uint64_t* mbar, uint32_t parity, int polls) {
+  for (int i = 0; i < polls; ++i)
+    if (__all_sync(0xffffffffu, phase_done(mbar, parity))) return true;
   return false;
+}
+
+// The wait for a load still in flight after a wait gave up: bounded by time
+// (kDrainNs of the global timer), so that it ends however long each poll
+// suspends the thread. The warp decides together, as above.
+constexpr unsigned long long kDrainNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool drain_phase_warp(uint64_t* mbar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (__all_sync(0xffffffffu, phase_done(mbar, parity))) return true;
+    const unsigned long long dt = global_ns() - t0;  // lane 0's clock decides for the warp
+    if (__shfl_sync(0xffffffffu, dt, 0) > kDrainNs) return false;
+  }
 }
 
 __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
@@ -485,12 +511,15 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
   if (!kCached) pdl_wait();  // the layout kernel's route codes
 
   uint32_t parity = 0;
-  int gt = gwarp;
-  for (; gt < p.total_tokens; gt += nwarps) {
+  // false once a wait of this warp gave up: the warp then writes only the
+  // receipts of its remaining tokens (valid codes, so that the combine never
+  // reads outside the arenas) and moves no more rows
+  bool copying = true;
+  for (int gt = gwarp; gt < p.total_tokens; gt += nwarps) {
     const int s = source_of_token(p, gt);
     const SourceDesc& src = p.src[s];
     const int t = gt - src.tok_off;
-    if (gt != gwarp && lane == 0) bulk_load(buf, src.x + (int64_t)t * rb, rb, mbar);
+    if (copying && gt != gwarp && lane == 0) bulk_load(buf, src.x + (int64_t)t * rb, rb, mbar);
     int code = -1;
     if (kCached) {
       if (lane < K) {
@@ -520,21 +549,21 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
           p.row_scales[((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.nscale + b] = sc;
       }
     }
-    const bool arrived = wait_phase(mbar, parity);
-    if (!arrived) break;
+    if (!copying) continue;
+    if (!wait_phase_warp(mbar, parity, p.wait_polls)) {
+      // the row's load did not complete in time: report it, and wait (bounded
+      // by time) for the load still in flight before the buffer is abandoned
+      if (lane == 0) atomicMin(p.err, route_error_key(s, t, 0, kErrTimeout));
+      drain_phase_warp(mbar, parity);
+      copying = false;
+      continue;
+    }
     parity ^= 1u;
     if (code >= 0)
       bulk_store(p.rows + ((int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)) * rb, buf, rb);
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // this lane's copies have read buf
     __syncwarp();
-  }
-  if (gt < p.total_tokens) {  // a wait gave up: report it, give the load in flight one more bounded wait
-    if (lane == 0) {
-      const int s = source_of_token(p, gt);
-      atomicMin(p.err, route_error_key(s, gt - p.src[s].tok_off, 0, kErrTimeout));
-    }
-    wait_phase(mbar, parity);
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this lane's copies are complete
   if (!kCached) fill_padding(p, p.ends);

@@ -55,6 +55,7 @@ constexpr int kSharedCarveout = 50;  // percent of the maximum shared memory
 constexpr int kErrRange = 5;    // AFD_ERR_ROUTE_RANGE
 constexpr int kErrDup = 6;      // AFD_ERR_ROUTE_DUP
 constexpr int kErrTimeout = 11; // AFD_ERR_TIMEOUT
+constexpr int kDefaultWaitPolls = 1 << 22;  // see afd_set_wait_limit
 constexpr int kBulkRowMax = 8192;  // rows up to this many bytes take the bulk-copy scatter
 constexpr unsigned long long kNoError = ~0ull;
 
@@ -86,6 +87,7 @@ struct DispatchParams {
   int32_t total_tokens;  // sum of T
   int32_t layout_ctas;   // CTAs of the layout cluster (large path)
   int32_t x_device;      // 1 when every source's rows are in device memory (bulk copies allowed)
+  int32_t wait_polls;    // polls of a bulk row load before the scatter gives up (AFD_ERR_TIMEOUT)
   int64_t R_arena;       // rows per worker arena
   // context scratch
   int32_t* route_tmp;    // [total_tokens][K]: the layout's route codes, (worker << 24) | row, or -1

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
 #include <mutex>
 
 #include "afd.h"
@@ -37,7 +38,7 @@ constexpr int kNaMaxDevices = 64;
 // word 64, then per-chunk counts [chunks][E], then route ranks [T*K].
 constexpr int kNaCountsOff = 64;
 constexpr int kNaRanksOff = kNaCountsOff + kNaMaxChunks * kNaMaxExperts;
-constexpr int kNaScratchWords = kNaRanksOff + kNaMaxRoutes;  // 393,280 words = 1.5 MiB
+constexpr int kNaScratchWords = kNaRanksOff + kNaMaxRoutes;  // 98,368 words = 384 KiB
 
 static __device__ __align__(256) int32_t g_layout_scratch[kNaScratchWords];
 
@@ -225,6 +226,14 @@ extern "C" AFD_API afd_status afd_route_layout_noalloc(const int64_t* ids, int32
     return AFD_ERR_ARG;
   if (T > kNaMaxTokens || K > kNaMaxTopK || E > kNaMaxExperts || (int64_t)T * K > kNaMaxRoutes)
     return AFD_ERR_UNSUPPORTED;
+  // Every row index inside a worker, and every intermediate sum of the
+  // aligned scan, is at most align_up(T*K + (E/F)*(alpha-1), alpha); it must
+  // fit the int32 arithmetic of the kernels.
+  {
+    const int64_t a = expert_alignment;
+    const int64_t bound = ((int64_t)T * K + (int64_t)(E / F) * (a - 1) + a - 1) / a * a;
+    if (bound > INT32_MAX) return AFD_ERR_UNSUPPORTED;
+  }
   if ((T > 0 && (!device_view(ids, &ids) || !device_view(slots, &slots))) || !device_view(ends, &ends) ||
       !device_view(error, &error))
     return AFD_ERR_ARG;
@@ -234,12 +243,26 @@ extern "C" AFD_API afd_status afd_route_layout_noalloc(const int64_t* ids, int32
   if (st != AFD_OK) return st;
 
   // The error key must start at "none" on every call; counts and ranks are
-  // overwritten in full.
+  // overwritten in full. Each step's own return code decides the status, so
+  // an error left pending by unrelated earlier work is neither reported here
+  // nor taken from its owner.
   if (cudaMemsetAsync(scratch, 0xff, sizeof(unsigned long long), stream) != cudaSuccess)
     return AFD_ERR_CUDA;
   const int G = (T + kNaChunk - 1) / kNaChunk;
-  if (G > 0)
-    na_count_kernel<<<G, kNaChunk, (size_t)kNaWarps * E * 6, stream>>>(ids, T, K, E, scratch);
-  na_finish_kernel<<<1, 1024, 0, stream>>>(T, K, E, F, expert_alignment, scratch, ends, slots, error);
-  return cudaGetLastError() == cudaSuccess ? AFD_OK : AFD_ERR_CUDA;
+  if (G > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kNaChunk);
+    cfg.dynamicSmemBytes = (size_t)kNaWarps * E * 6;
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, na_count_kernel, ids, T, K, E, scratch) != cudaSuccess) return AFD_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = stream;
+  if (cudaLaunchKernelEx(&cfg, na_finish_kernel, T, K, E, F, (int)expert_alignment, scratch, ends, slots,
+                         error) != cudaSuccess)
+    return AFD_ERR_CUDA;
+  return AFD_OK;
 }

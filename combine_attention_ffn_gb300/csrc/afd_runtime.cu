@@ -39,6 +39,7 @@ struct afd_ctx {
   int sm_count;
   int sm_cap;
   int layout_max_ctas;  // largest layout cluster this device runs
+  int wait_polls;       // polls of a bulk row load before the scatter gives up
   int Ef;
   int row_bytes;
   int nscale;
@@ -292,6 +293,7 @@ afd_status launch_exchange_dispatch(afd_ctx* c, cudaStream_t stream, bool cached
   p.nscale = c->nscale;
   p.total_tokens = tok;
   p.R_arena = c->R_arena;
+  p.wait_polls = c->wait_polls;
   p.route_tmp = c->route_tmp;
   p.layout_ctas = afd::layout_ctas_for(tok, c->sm_cap, c->layout_max_ctas);
   p.err = c->err;
@@ -423,6 +425,7 @@ afd_status afd_create(const afd_config* config, int32_t device, afd_ctx** out) {
     return AFD_ERR_CUDA;
   }
   c->gen = 1;
+  c->wait_polls = afd::kDefaultWaitPolls;
   reset_exchange(c);
   *out = c;
   return AFD_OK;
@@ -837,6 +840,13 @@ afd_status afd_get_error(afd_ctx* c, int32_t* code, int32_t* source, int32_t* to
   if (source) *source = none ? -1 : (int32_t)(key >> 56);
   if (token) *token = none ? -1 : (int32_t)((key >> 16) & 0xffffffffull);
   if (k) *k = none ? -1 : (int32_t)((key >> 8) & 0xff);
+  return AFD_OK;
+}
+
+afd_status afd_set_wait_limit(afd_ctx* c, int32_t polls) {
+  if (!c) return AFD_ERR_ARG;
+  if (polls < 0) return fail(c, AFD_ERR_ARG, "polls must be >= 0");
+  c->wait_polls = polls;
   return AFD_OK;
 }
 

@@ -273,10 +273,24 @@ AFD_API afd_status afd_source_collect_all(afd_ctx* ctx, void* const* outs, int32
  * (source, token, k) is the invalid route that comes first in (source,
  * token, k) order among all exchanges since the last afd_clear_error), or
  * AFD_ERR_TIMEOUT (a bounded wait of the scatter's bulk copies gave up at
- * (source, token); k = 0). Any pointer may be NULL. Not allowed while the
- * context's last stream is capturing (AFD_ERR_CAPTURING). */
+ * (source, token); k = 0; see afd_set_wait_limit). Any pointer may be NULL.
+ * Not allowed while the context's last stream is capturing
+ * (AFD_ERR_CAPTURING). */
 AFD_API afd_status afd_get_error(afd_ctx* ctx, int32_t* code, int32_t* source, int32_t* token,
                          int32_t* k);
+
+/* Sets how many times the scatter polls for each source row's bulk load
+ * before it gives up (default 4,194,304, each poll possibly suspending the
+ * thread for a while). A load that does not complete in time is reported
+ * through afd_get_error as AFD_ERR_TIMEOUT at that row's (source, token); the
+ * warp that gave up waits for the load still in flight (up to 2 s of GPU
+ * time), moves no more rows but still writes every receipt, so the rest of
+ * the exchange runs and its outputs are unspecified. 0 makes every first
+ * wait give up at once: a way to exercise that error path. Applies to
+ * dispatches enqueued after the call (a captured graph keeps the value it
+ * was captured with).
+ * Errors: AFD_ERR_ARG (polls < 0). */
+AFD_API afd_status afd_set_wait_limit(afd_ctx* ctx, int32_t polls);
 
 /* Clears the sticky route error (enqueued on `stream`). */
 AFD_API afd_status afd_clear_error(afd_ctx* ctx, afd_stream stream);
@@ -301,7 +315,7 @@ AFD_API int64_t afd_recv_rows_for_bucket(const afd_ctx* ctx, int32_t bucket);
  * callers cannot call cudaMalloc: code that runs inside another framework's
  * memory pool or allocator hook, or a process whose device memory is fully
  * reserved up front. This call allocates nothing, through the CUDA runtime or
- * any library: its scratch (about 1.5 MiB) is a fixed device array inside
+ * any library: its scratch (384 KiB) is a fixed device array inside
  * libafd, which every GPU that loads the library holds until the process
  * exits. It computes, for one source's routing, what the dispatch layout
  * computes: route checks, per-worker ends[] with expert_alignment padding,
@@ -316,8 +330,10 @@ AFD_API int64_t afd_recv_rows_for_bucket(const afd_ctx* ctx, int32_t bucket);
  *              route in (token, k) order (code AFD_ERR_ROUTE_RANGE or
  *              AFD_ERR_ROUTE_DUP), or {AFD_OK, -1, -1}
  * Limits: num_tokens <= 8192, top_k <= 32, num_tokens * top_k <= 65536,
- * num_experts <= 1024; larger sizes return AFD_ERR_UNSUPPORTED and enqueue
- * nothing. Every buffer must be reachable from the current device (its
+ * num_experts <= 1024, and align_up(num_tokens * top_k + (E/F) *
+ * (expert_alignment - 1), expert_alignment) <= INT32_MAX (the largest row
+ * index of a worker must fit an int32); larger sizes return
+ * AFD_ERR_UNSUPPORTED and enqueue nothing. Every buffer must be reachable from the current device (its
  * device memory, managed memory, or page-locked host memory); pageable host
  * memory or another device's memory returns AFD_ERR_ARG and enqueues
  * nothing. Work is enqueued on `stream` (the current device's).

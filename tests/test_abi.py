@@ -92,3 +92,21 @@ def test_missing_library_fails_loudly(tmp_path):
 
     with pytest.raises(afd.AfdError):
         afd.load_library(str(tmp_path / "libafd.so"))
+
+
+def test_noalloc_size_limits_are_host_checks(lib_path):
+    """afd_route_layout_noalloc refuses sizes beyond its fixed scratch, and
+    alignments whose largest row index would overflow int32, on the host
+    before any CUDA call (so this runs without a GPU)."""
+    from combine_attention_ffn_gb300 import afd
+
+    lib = afd.load_library(lib_path)
+    bogus = ctypes.c_void_p(16)
+    for T, K, E, F, alpha in ((8193, 1, 16, 2, 4), (4096, 17, 32, 2, 1), (64, 8, 1025, 1, 1),
+                              (8192, 8, 1024, 1, 1 << 21), (0, 1, 1024, 1, (1 << 31) - 1)):
+        st = lib.afd_route_layout_noalloc(bogus, T, K, E, F, alpha, bogus, bogus, bogus, None)
+        assert st == afd.ERR_UNSUPPORTED, (T, K, E, F, alpha)
+    for T, K, E, F, alpha in ((-1, 1, 8, 1, 1), (4, 0, 8, 1, 1), (4, 9, 8, 1, 1), (4, 2, 9, 2, 1),
+                              (4, 2, 8, 2, 0)):
+        st = lib.afd_route_layout_noalloc(bogus, T, K, E, F, alpha, bogus, bogus, bogus, None)
+        assert st == afd.ERR_ARG, (T, K, E, F, alpha)

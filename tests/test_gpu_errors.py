@@ -178,3 +178,41 @@ def test_read_host_counts_during_capture_is_refused():
         del g
     finally:
         buf.close()
+
+
+@pytest.mark.parametrize("name,T", [("2A2F", 512), ("fp8-2A2F", 300)])
+def test_scatter_wait_that_gives_up_is_reported_and_recoverable(name, T):
+    """The bulk-copy scatter waits a bounded number of polls for each source
+    row's load. With the limit at 0 every warp's first wait gives up at once:
+    the scatter reports AFD_ERR_TIMEOUT at the first token in (source, token)
+    order, waits for the load still in flight, and writes every receipt
+    anyway, so the receive side is the oracle's layout and the combine reads
+    only rows inside the arenas. The context then runs a correct exchange."""
+    wl = W.named(name, T=T)
+    inp = W.make_inputs(wl)
+    assert sum(wl.T) * wl.K > 2048 and sum(wl.T) > 32  # the layout + bulk-scatter path
+    exp = GH.expected(inp, GH.SCALE)
+    buf = GH.make_buffer(wl)
+    try:
+        dev = GH.to_device(inp)
+        buf.set_wait_limit(0)
+        recvs, _, _ = GH.run_exchange(buf, wl, dev)
+        snap = GH.snapshot(recvs)
+        torch.cuda.synchronize()
+        assert buf.get_error() == (afd.ERR_TIMEOUT, 0, 0, 0)
+        for f in range(wl.F):
+            R = int(exp["r_exact"][f])
+            assert np.array_equal(snap[f]["ends"], exp["ends"][f])
+            assert np.array_equal(snap[f]["row_src"][:R], exp["row_src"][f, :R])
+            assert np.array_equal(snap[f]["weights"][:R].view(np.uint32),
+                                  exp["row_w"][f, :R].view(np.uint32))
+        with pytest.raises(afd.AfdError):
+            buf.set_wait_limit(-1)
+        buf.set_wait_limit(1 << 22)
+        buf.clear_error()
+        recvs, _, results = GH.run_exchange(buf, wl, dev)
+        GH.check_layout(wl, GH.snapshot(recvs), exp, False, buf)
+        GH.check_outputs(wl, results, exp)
+        assert buf.get_error() == (0, -1, -1, -1)
+    finally:
+        buf.close()
