@@ -31,10 +31,36 @@ import numpy as np  # noqa: E402
 METRIC = "dispatch+combine µs/round trip; achieved HBM GB/s vs peak (E128 K8 H2048)"
 COMBINE_MODES = {"fused": 0, "two-stage": 1, "two-stage-fp8": 2}  # afd_config.combine_mode
 FALLBACK_HBM_GBS = 6800.0
-PAGES_CONTEXT_US = {  # afdEP-comm design page, "Result" table: 4 x H100 NVLink, communication only
-    ("2A2F", 2048, 1): 20.7, ("2A2F", 2048, 2048): 192.7,
-    ("2A2F-H4096", 4096, 1): 28.4, ("2A2F-H4096", 4096, 2048): 383.2,
+# afdEP-comm design page, "Result" table: round trip in us, afdEP-comm (FastAFD M2N),
+# 4 x H100 in one NVLink domain, communication only, random routing, CUDA graphs,
+# 24 transport SMs, at T = 1, 8, 32, 128, 512, 2048 tokens per source. Context
+# for the rows of the same layout, hidden size and dtype; not a target (other
+# hardware, a multi-GPU transport).
+PAGES_T = (1, 8, 32, 128, 512, 2048)
+PAGES_RESULT_US = {
+    "2A2F, H2048, BF16": ((20.7, 31.7), (24.8, 34.4), (26.3, 36.0), (35.3, 44.3), (70.6, 78.7), (192.7, 201.0)),
+    "2A2F, H4096, BF16": ((28.4, 39.1), (39.2, 47.9), (46.3, 55.7), (61.5, 68.7), (127.3, 136.2), (383.2, 392.6)),
+    "3A:1F, H2048, BF16": ((24.8, 36.4), (27.4, 38.6), (33.0, 44.8), (45.9, 55.8), (109.4, 119.5), (367.8, 372.1)),
+    "1A:3F (E96), H2048, BF16": ((19.9, 30.5), (21.5, 31.3), (23.1, 32.8), (29.4, 39.7), (59.6, 67.7), (188.3, 197.7)),
+    "2A2F, H2048, FP8 dispatch": ((21.3, 32.3), (25.9, 35.6), (26.8, 36.7), (34.5, 43.5), (62.5, 71.8), (159.1, 167.8)),
 }
+PAGES_ROW_OF = {"2A2F": "2A2F, H2048, BF16", "2A2F-H4096": "2A2F, H4096, BF16",
+                "skew-3A1F": "3A:1F, H2048, BF16", "skew-1A3F": "1A:3F (E96), H2048, BF16",
+                "fp8-2A2F": "2A2F, H2048, FP8 dispatch"}
+
+
+def pages_context(name: str, T: int, combine: str = "fused"):
+    """The pages' cell for this layout and token count, or None."""
+    row = PAGES_ROW_OF.get(name)
+    if row is None or T not in PAGES_T:
+        return None
+    ours, base = PAGES_RESULT_US[row][PAGES_T.index(T)]
+    note = "4 x H100 NVLink, communication only, random routing; context, not a target"
+    if name.startswith("skew"):
+        note += " (this row's routing is skewed)"
+    if combine != "fused":
+        note += " (the pages' cell rounds per FFN rank like this row)"
+    return {"pages_row": row, "afdEP_comm_us": ours, "fastafd_m2n_us": base, "note": note}
 
 
 def parse_args():
@@ -56,7 +82,7 @@ def parse_args():
                     help="time the exchange and a side-stream GEMM batch alone and together "
                          "(the pages' synthetic compute load) and print that record instead")
     ap.add_argument("--all-configs", action="store_true",
-                    help="time every workload at each of its token counts and print that table")
+                    help="print only the sweep of every workload (no headline)")
     ap.add_argument("--profile-exchanges", type=int, default=0,
                     help="run this many eager exchanges of the workload and exit "
                          "(a short, untimed program for an external profiler)")
@@ -227,7 +253,11 @@ def dist_env():
 
 # ------------------------------------------------------------------ reference arm
 def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1, combine_mode: str = "fused"):
-    """Times the oracle's dispatch + combine (identity expert) on this host."""
+    """Times the oracle's round trip on this host: validate, layout, dispatch
+    and combine. The expert between dispatch and combine is harness work on
+    both sides (identity: the replies are the received rows; FP8: the rows
+    dequantised to BF16 by the oracle's stand-in) and is not timed, as on the
+    GPU side."""
     import oracle
 
     p = oracle.Problem(wl.A, wl.F, wl.E, wl.K, wl.H, wl.alpha, wl.bucket,
@@ -240,14 +270,25 @@ def cpu_oracle_round_trip_us(wl, inp, budget_s: float, min_reps: int = 1, combin
         lay = oracle.layout(p, inp.ids)
         r_stride = max(1, int(lay["r_exact"].max()))
         d = oracle.dispatch(p, inp.ids, inp.w, inp.x, inp.x_scales, lay, r_stride)
-        reply = d["rows"].view(np.uint16).reshape(wl.F, r_stride, wl.H)
+        t1 = time.perf_counter()
+        if wl.dtype == "fp8":
+            reply = oracle.expert(p, oracle.EXPERT_IDENTITY, lay, r_stride, d["rows"], d["row_scales"])
+        else:
+            reply = d["rows"].view(np.uint16).reshape(wl.F, r_stride, wl.H)
+        t2 = time.perf_counter()
         if combine_mode == "fused":
             oracle.combine(p, inp.ids, inp.w, d["slot"], r_stride, reply)
         else:
             oracle.combine_two_stage(p, inp.ids, inp.w, d["slot"], r_stride, reply,
                                      fp8=combine_mode == "two-stage-fp8")
-        times.append((time.perf_counter() - t0) * 1e6)
+        t3 = time.perf_counter()
+        times.append(((t1 - t0) + (t3 - t2)) * 1e6)
     return times
+
+
+def oracle_reps(T: int) -> int:
+    """Repeats of the per-row oracle timing: 3, or 5 for small batches."""
+    return 5 if T <= 128 else 3
 
 
 def run_reference(args):
@@ -258,9 +299,6 @@ def run_reference(args):
         return 0
     wl = W.named(args.config, T=args.tokens)
     inp = W.make_inputs(wl)
-    if wl.dtype == "fp8":
-        print(json.dumps({"impl": "reference", "unavailable": "the CPU arm times BF16 workloads only"}))
-        return 0
     cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.warmup, combine_mode=args.combine_mode)  # warm-up
     steps = cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=args.steps, combine_mode=args.combine_mode)
     value = statistics.mean(steps)
@@ -270,8 +308,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, execution="CPU oracle (single-threaded C) on the host",
-                                  l2="not applicable", combine=args.combine_mode),
+        "config": workload_config(wl, combine=args.combine_mode),
+        "execution": "CPU oracle (single-threaded C) on the host; the expert stand-in is not timed",
+        "l2": "not applicable",
         "gbs": round(ab["total"] / (value * 1e-6) / 1e9, 2),
         "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full round trips of the workload, single-threaded C oracle",
@@ -283,95 +322,208 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl, execution: str = "one CUDA graph per round trip",
-                    l2: str = "flushed before every timed step (256 MB write, then 256 MB read so the "
-                              "write-backs finish first; outside the step's events)",
-                    combine: str = "fused") -> dict:
+L2_NOTE = ("flushed before every timed step (256 MB write, then 256 MB read so the write-backs "
+           "finish first; outside the step's events)")
+
+
+def workload_config(wl, combine: str = "fused") -> dict:
     return {"workload": f"{wl.name}: A={wl.A} sources x T={wl.T[0]} tokens, F={wl.F} workers, "
                         f"E={wl.E}, K={wl.K}, H={wl.H}, {wl.dtype}, alpha={wl.alpha}, "
                         f"bucket={wl.bucket}, {wl.routing} routing",
             "A": wl.A, "F": wl.F, "E": wl.E, "K": wl.K, "H": wl.H, "T_per_source": wl.T[0],
             "bucket": wl.bucket, "expert_alignment": wl.alpha, "routing": wl.routing,
-            "expert": "identity (reply = received rows)", "combine": combine,
-            "l2": l2, "execution": execution}
+            "expert": "identity (reply = received rows)" if wl.dtype == "bf16" else
+                      "BF16 replies computed once from the received rows, outside the timed graph",
+            "combine": combine}
 
 
 # ------------------------------------------------------------------ our arm
-def run_under_load(args):
+class Rig:
+    """One workload's exchange, ready to replay: inputs resident in device
+    memory, the context, and the BF16 replies. BF16 replies are the received
+    rows (identity expert, as in the pages' communication-only numbers); FP8
+    replies are the received rows dequantised to BF16 once, from a first
+    exchange outside any timed region (routing and rows do not change between
+    replays, so they stay the right replies)."""
+
+    def __init__(self, torch, afd, W, name, T, dev, combine="fused", num_sms=0):
+        self.torch = torch
+        wl = self.wl = W.named(name, T=T)
+        inp = self.inp = W.make_inputs(wl)
+        self.buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
+                              num_sms=num_sms, combine_mode=COMBINE_MODES[combine])
+        fp8 = self.fp8 = wl.dtype == "fp8"
+        if fp8:
+            self.xs = [torch.from_numpy(inp.x[s, :t].copy()).to(dev).view(torch.float8_e4m3fn)
+                       for s, t in enumerate(wl.T)]
+            self.scs = [torch.from_numpy(inp.x_scales[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+        else:
+            self.xs = [torch.from_numpy(inp.x[s, :t].view(np.int16).copy()).to(dev).view(torch.bfloat16)
+                       for s, t in enumerate(wl.T)]
+            self.scs = [None] * wl.A
+        self.ids = [torch.from_numpy(inp.ids[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+        self.ws = [torch.from_numpy(inp.w[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
+        self.outs = [torch.empty((t, wl.H), dtype=torch.bfloat16, device=dev) for t in wl.T]
+        self.replies = None
+        if fp8:
+            replies = {}
+
+            def expert(f, r):
+                v = r.rows.float() * r.row_scales.repeat_interleave(128, dim=1)
+                replies[f] = v.to(torch.bfloat16).contiguous()
+                return replies[f]
+
+            self.exchange(expert=expert)
+            torch.cuda.synchronize()
+            self.replies = replies
+
+    def exchange(self, view=False, cached=False, batched=False, expert=None):
+        wl, buf = self.wl, self.buf
+        for s in range(wl.A):
+            if cached:
+                buf.source_dispatch_cached(s, self.xs[s], self.ws[s], self.scs[s], bucket=wl.bucket)
+            else:
+                buf.source_dispatch(s, self.xs[s], self.ids[s], self.ws[s], self.scs[s], bucket=wl.bucket)
+        for f in range(wl.F):
+            r = buf.worker_receive(f, bucket=wl.bucket)
+            reply = expert(f, r) if expert else (self.replies[f] if self.fp8 else r.rows)
+            buf.worker_reply(f, reply, r.receipt)
+        if batched:
+            buf.source_collect_all(view=view, outs=None if view and wl.F == 1 else self.outs)
+        else:
+            for s in range(wl.A):
+                buf.source_collect(s, out=None if view and wl.F == 1 else self.outs[s], view=view)
+
+    def graph(self, **kw):
+        """One exchange captured as a CUDA graph (after one eager exchange)."""
+        torch = self.torch
+        self.exchange(**kw)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.exchange(**kw)
+        return g
+
+    def close(self):
+        self.buf.close()
+
+
+def replay_stats(torch, g, flush, n_flushed: int = 10, n_btb: int = 50):
+    """Median µs of one replay with L2 flushed before it (outside its events),
+    and mean µs of n_btb replays back to back."""
+    for _ in range(3):
+        g.replay()
+    times = []
+    for _ in range(n_flushed):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n_btb):
+        g.replay()
+    b.record()
+    b.synchronize()
+    return statistics.median(times), a.elapsed_time(b) * 1e3 / n_btb
+
+
+# Rows of the default run: every workload at the token counts of its
+# benchmark, and the pages' per-worker rounding (two-stage combine).
+SWEEP = (("tiny", (16,), "fused"), ("2A2F", (1, 8, 32, 128, 512, 2048), "fused"),
+         ("2A2F-H4096", (1, 128, 2048), "fused"), ("skew-3A1F", (1, 32, 512, 2048), "fused"),
+         ("skew-1A3F", (1, 32, 512, 2048), "fused"), ("fp8-2A2F", (1, 128, 2048), "fused"),
+         ("fp8-2A1F", (1, 128, 2048), "fused"),
+         ("2A2F", (1, 128, 512, 2048), "two-stage"), ("2A2F", (1, 128, 512, 2048), "two-stage-fp8"))
+
+
+def measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=True):
+    """Every row of SWEEP, one CUDA graph replay per round trip: µs after an
+    L2 flush and back to back, algorithmic bytes, GB/s and the fraction of
+    the HBM peak (from 512 tokens per source; below, the round trip is bound
+    by latency), the pages' cell for the same layout as context, and the
+    oracle's time for the same round trip on this host. Single-worker
+    layouts also collect through the view; the 2A2F layouts also with a
+    cached dispatch and with one batched collect."""
+    rows = []
+    for name, Ts, mode in SWEEP:
+        for T in Ts:
+            rig = Rig(torch, afd, W, name, T, dev, combine=mode)
+            wl, inp = rig.wl, rig.inp
+            variants = [("full", {})]
+            if wl.F == 1:
+                variants.append(("view", dict(view=True)))
+            if name in ("2A2F", "2A2F-H4096") and mode == "fused":
+                variants += [("cached", dict(cached=True)), ("batched collect", dict(batched=True))]
+            for label, kw in variants:
+                g = rig.graph(**kw)
+                us, btb = replay_stats(torch, g, flush)
+                del g
+                ab = algorithmic_bytes(wl, inp, view=kw.get("view", False))
+                gbs = ab["total"] / (us * 1e-6) / 1e9
+                row = {"config": name, "T": T, "combine": mode, "variant": label, "us": round(us, 2),
+                       "us_back_to_back": round(btb, 2), "bytes": int(ab["total"]), "gbs": round(gbs, 1),
+                       "frac": round(gbs / peak, 4) if T >= 512 else None}
+                if label == "full":
+                    row["context"] = pages_context(name, T, mode)
+                    if with_oracle:
+                        n = oracle_reps(T)
+                        row["oracle_us"] = round(statistics.median(
+                            cpu_oracle_round_trip_us(wl, inp, 0.0, min_reps=n, combine_mode=mode)), 1)
+                        row["oracle_reps"] = n
+                rows.append(row)
+            torch.cuda.synchronize()
+            rig.close()
+    return rows
+
+
+def measure_under_load(torch, afd, W, dev, name="2A2F", Ts=(512, 2048), settings=((0, False), (24, False)),
+                       n_ex: int = 100, n_gemm: int = 100):
     """The exchange under compute load (afdEP-comm design page, section 14:
     a fixed batch of 2,048^3 BF16 GEMMs on a side stream while the exchanges
-    replay). For each token count and SM cap: GEMM time alone and under the
-    exchange, exchange time alone and under the GEMMs, and the makespan."""
-    import torch
-
-    from combine_attention_ffn_gb300 import afd
-    from combine_attention_ffn_gb300 import build as libbuild
-    from combine_attention_ffn_gb300 import workloads as W
-
-    libbuild.build()
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    replay). Per token count and (SM cap, exchange stream priority): GEMM time
+    alone and under the exchanges, exchange time alone and under the GEMMs,
+    and the makespan of both."""
     side_s = torch.cuda.Stream()
     a = torch.randn(2048, 2048, device=dev, dtype=torch.bfloat16)
     b = torch.randn(2048, 2048, device=dev, dtype=torch.bfloat16)
     c = torch.empty(2048, 2048, device=dev, dtype=torch.bfloat16)
-    n_ex, n_gemm = 200, 200
-
-    main_s = torch.cuda.current_stream()
-
-    def span(fn_main, fn_side):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        torch.cuda.synchronize()
-        e[0].record(main_s)
-        side_s.wait_event(e[0])
-        if fn_side:
-            with torch.cuda.stream(side_s):
-                e[2].record(side_s)
-                fn_side()
-                e[3].record(side_s)
-        if fn_main:
-            fn_main()
-        e[1].record(main_s)
-        torch.cuda.synchronize()
-        t_main = e[0].elapsed_time(e[1]) * 1e3 if fn_main else None
-        t_side = e[2].elapsed_time(e[3]) * 1e3 if fn_side else None
-        make = max(e[0].elapsed_time(e[1]), e[0].elapsed_time(e[3]) if fn_side else 0) * 1e3
-        return t_main, t_side, make
 
     def gemms():
         for _ in range(n_gemm):
             torch.matmul(a, b, out=c)
 
     rows = []
-    for T in (1, 32, 512, 2048):
-        wl = W.named(args.config, T=T)
-        inp = W.make_inputs(wl)
-        xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
-              for s in range(wl.A)]
-        ids = [torch.from_numpy(inp.ids[s, :T].copy()).to(dev) for s in range(wl.A)]
-        ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s in range(wl.A)]
-        outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(wl.A)]
-        for sms, prio in ((0, False), (64, False), (24, False), (0, True)):
-            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype, num_sms=sms)
-            # the exchange's stream: the default one, or one of the highest priority
+    for T in Ts:
+        for sms, prio in settings:
+            rig = Rig(torch, afd, W, name, T, dev, num_sms=sms)
             main_s = torch.cuda.Stream(priority=torch.cuda.Stream.priority_range()[1]) if prio \
                 else torch.cuda.default_stream()
             torch.cuda.set_stream(main_s)
 
-            def exchange():
-                for s in range(wl.A):
-                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
-                for f in range(wl.F):
-                    r = buf.worker_receive(f, bucket=wl.bucket)
-                    buf.worker_reply(f, r.rows, r.receipt)
-                for s in range(wl.A):
-                    buf.source_collect(s, out=outs[s])
+            def span(fn_main, fn_side):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                torch.cuda.synchronize()
+                e[0].record(main_s)
+                side_s.wait_event(e[0])
+                if fn_side:
+                    with torch.cuda.stream(side_s):
+                        e[2].record(side_s)
+                        fn_side()
+                        e[3].record(side_s)
+                if fn_main:
+                    fn_main()
+                e[1].record(main_s)
+                torch.cuda.synchronize()
+                t_main = e[0].elapsed_time(e[1]) * 1e3 if fn_main else None
+                t_side = e[2].elapsed_time(e[3]) * 1e3 if fn_side else None
+                make = max(e[0].elapsed_time(e[1]), e[0].elapsed_time(e[3]) if fn_side else 0) * 1e3
+                return t_main, t_side, make
 
-            exchange()
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                exchange()
+            g = rig.graph()
 
             def replays():
                 for _ in range(n_ex):
@@ -389,29 +541,14 @@ def run_under_load(args):
                          "gemm_slowdown": round(gemm_load / gemm_alone - 1, 4),
                          "makespan_ms": round(make / 1e3, 3)})
             del g
-            buf.close()
+            rig.close()
             torch.cuda.set_stream(torch.cuda.default_stream())
-    print(json.dumps({"metric": "exchange and side-stream GEMM under load", "mode": "under_load",
-                      "config": {"workload": args.config, "gemm": "2048^3 BF16 (torch.matmul) x 200",
-                                 "exchanges": n_ex, "execution": "one CUDA graph per exchange"},
-                      "rows": rows}))
-    return 0
+    return rows
 
 
-ALL_CONFIGS = (("tiny", (16,), "fused"), ("2A2F", (1, 8, 32, 128, 512, 2048), "fused"),
-               ("2A2F-H4096", (1, 128, 2048), "fused"), ("skew-3A1F", (1, 32, 512, 2048), "fused"),
-               ("skew-1A3F", (1, 32, 512, 2048), "fused"), ("fp8-2A2F", (1, 128, 2048), "fused"),
-               ("fp8-2A1F", (1, 128, 2048), "fused"),
-               # the pages' per-worker rounding (two-stage combine), BF16 and E4M3 partials
-               ("2A2F", (1, 128, 512, 2048), "two-stage"), ("2A2F", (1, 128, 512, 2048), "two-stage-fp8"))
-
-
-def run_all_configs(args):
-    """Every workload at each of its token counts, one CUDA graph replay per
-    step, L2 flushed before each replay. BF16: the whole round trip with the
-    identity expert. FP8: the replies need an expert (BF16 from the E4M3 rows
-    and scales), which runs untimed between two graphs: dispatch + receive,
-    then reply + collect; the value is their sum."""
+def run_under_load(args):
+    """The full under-load table (more token counts and settings than the
+    default run's block)."""
     import torch
 
     from combine_attention_ffn_gb300 import afd
@@ -421,107 +558,33 @@ def run_all_configs(args):
     libbuild.build()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    flush = L2Flush(torch, dev)
-    peak, peak_kind = load_peaks()
-
-    def timed(fn, n=15):
-        times = []
-        for _ in range(n):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            times.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(times)
-
-    rows = []
-    for name, Ts, mode in ALL_CONFIGS:
-        for T in Ts:
-            wl = W.named(name, T=T)
-            inp = W.make_inputs(wl)
-            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
-                             combine_mode=COMBINE_MODES[mode])
-            fp8 = wl.dtype == "fp8"
-            if fp8:
-                xs = [torch.from_numpy(inp.x[s, :t].copy()).to(dev).view(torch.float8_e4m3fn)
-                      for s, t in enumerate(wl.T)]
-                scs = [torch.from_numpy(inp.x_scales[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
-            else:
-                xs = [torch.from_numpy(inp.x[s, :t].view(np.int16).copy()).to(dev).view(torch.bfloat16)
-                      for s, t in enumerate(wl.T)]
-                scs = [None] * wl.A
-            ids = [torch.from_numpy(inp.ids[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
-            ws_ = [torch.from_numpy(inp.w[s, :t].copy()).to(dev) for s, t in enumerate(wl.T)]
-            outs = [torch.empty((t, wl.H), dtype=torch.bfloat16, device=dev) for t in wl.T]
-            recv = {}
-            replies = {}
-
-            def first_half():
-                for s in range(wl.A):
-                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], scs[s], bucket=wl.bucket)
-                for f in range(wl.F):
-                    recv[f] = buf.worker_receive(f, bucket=wl.bucket)
-
-            def expert():
-                for f in range(wl.F):
-                    r = recv[f]
-                    if fp8:
-                        v = r.rows.float() * r.row_scales.repeat_interleave(128, dim=1)
-                        replies[f] = v.to(torch.bfloat16)
-                    else:
-                        replies[f] = r.rows
-
-            use_view = [False]
-
-            def second_half():
-                for f in range(wl.F):
-                    buf.worker_reply(f, replies[f], recv[f].receipt)
-                for s in range(wl.A):
-                    buf.source_collect(s, out=None if use_view[0] else outs[s], view=use_view[0])
-
-            for use_view[0] in ((False, True) if wl.F == 1 else (False,)):
-                first_half(); expert(); second_half()
-                torch.cuda.synchronize()
-                us = timed_exchange(fp8, first_half, expert, second_half, timed, torch)
-                ab = algorithmic_bytes(wl, inp, view=use_view[0])
-                gbs = ab["total"] / (us * 1e-6) / 1e9
-                rows.append({"config": name + (" view" if use_view[0] else "")
-                             + ("" if mode == "fused" else f" {mode}"), "T": T,
-                             "us": round(us, 2), "gbs": round(gbs, 1),
-                             "frac": round(gbs / peak, 4) if T >= 512 else None})
-            buf.close()
-    print(json.dumps({"metric": METRIC, "mode": "all_configs", "unit": "us", "peak_gbs": peak,
-                      "peak_kind": peak_kind, "native_digest": native_digest(),
-                      "l2": "flushed before every timed replay", "rows": rows}))
+    rows = measure_under_load(torch, afd, W, dev, args.config, Ts=(1, 32, 512, 2048),
+                              settings=((0, False), (64, False), (24, False), (0, True)),
+                              n_ex=200, n_gemm=200)
+    print(json.dumps({"metric": "exchange and side-stream GEMM under load", "mode": "under_load",
+                      "config": {"workload": args.config, "gemm": "2048^3 BF16 (torch.matmul) x 200",
+                                 "exchanges": 200, "execution": "one CUDA graph per exchange"},
+                      "rows": rows}))
     return 0
 
 
-def timed_exchange(fp8, first_half, expert, second_half, timed, torch):
-    """Graph-replayed exchange time; FP8 sums the two graphs around the expert."""
-    if fp8:
-        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1):
-            first_half()
-        expert()
-        with torch.cuda.graph(g2):
-            second_half()
-        g1.replay()
-        g2.replay()
-        us = timed(g1.replay) + timed(g2.replay)
-        del g1, g2
-    else:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            first_half()
-            expert()
-            second_half()
-        g.replay()
-        us = timed(g.replay)
-        del g
-    torch.cuda.synchronize()
-    return us
+def run_sweep_only(args):
+    """Only the sweep of every workload (no headline), as one JSON line."""
+    import torch
+
+    from combine_attention_ffn_gb300 import afd
+    from combine_attention_ffn_gb300 import build as libbuild
+    from combine_attention_ffn_gb300 import workloads as W
+
+    libbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = load_peaks()
+    rows = measure_sweep(torch, afd, W, dev, L2Flush(torch, dev), peak, with_oracle=not args.no_cpu_baseline)
+    print(json.dumps({"metric": METRIC, "mode": "sweep", "unit": "us", "peak_gbs": peak,
+                      "peak_kind": peak_kind, "native_digest": native_digest(), "l2": L2_NOTE,
+                      "host": host_cpu(), "rows": rows}))
+    return 0
 
 
 def main():
@@ -531,7 +594,7 @@ def main():
     if args.under_load:
         return run_under_load(args)
     if args.all_configs:
-        return run_all_configs(args)
+        return run_sweep_only(args)
 
     import warnings
 
@@ -560,7 +623,7 @@ def main():
         torch.distributed.barrier()
     wl = W.named(args.config, T=args.tokens)
     if wl.dtype == "fp8":
-        raise SystemExit("bench.py times the BF16 identity-expert round trip; FP8 needs an expert")
+        raise SystemExit("the headline times the BF16 identity-expert round trip; FP8 rows are in the sweep")
     inp = W.make_inputs(wl)
     buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
                      combine_mode=COMBINE_MODES[args.combine_mode])
@@ -650,6 +713,7 @@ def main():
     steps_ev = [(ev(), ev()) for _ in range(args.steps)]
     batched_ev = [(ev(), ev()) for _ in range(args.steps)]
     phase_ev = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    cold_ev = [[(ev(), ev()) for _ in range(3)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -665,6 +729,11 @@ def main():
         for j, gp in enumerate(g_phase):
             gp.replay()
             pe[j + 1].record()
+        for j, gp in enumerate(g_phase):  # each phase alone, L2 flushed before it
+            flush()
+            cold_ev[i][j][0].record()
+            gp.replay()
+            cold_ev[i][j][1].record()
         flush()
         batched_ev[i][0].record()
         g_batched.replay()
@@ -700,6 +769,8 @@ def main():
     d_ms = statistics.mean(pe[0].elapsed_time(pe[1]) for pe in phase_ev)
     r_ms = statistics.mean(pe[1].elapsed_time(pe[2]) for pe in phase_ev)
     c_ms = statistics.mean(pe[2].elapsed_time(pe[3]) for pe in phase_ev)
+    d_cold, r_cold, c_cold = (statistics.mean(ce[j][0].elapsed_time(ce[j][1]) for ce in cold_ev)
+                              for j in range(3))
 
     ab = algorithmic_bytes(wl, inp)
     peak, peak_kind = load_peaks()
@@ -723,6 +794,9 @@ def main():
     achieved = per_launch_bytes / per_launch_s / 1e9
     traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}") if args.combine_mode == "fused" else None
     d_gbs = ab["dispatch"] / (d_ms * 1e-3) / 1e9
+    comb_cold_s = (r_cold if wl.F == 1 else c_cold) / n_launch * 1e-3
+    cold_achieved = per_launch_bytes / comb_cold_s / 1e9
+    d_cold_gbs = ab["dispatch"] / (d_cold * 1e-3) / 1e9
     roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -733,7 +807,17 @@ def main():
                              "collect": round(c_ms * 1e3, 2)},
                 "dispatch_phase": {"us": round(d_ms * 1e3, 2), "bytes": int(ab["dispatch"]),
                                    "achieved": round(d_gbs, 1), "frac": round(d_gbs / peak, 4)},
-                "note": "per-phase graphs replayed after each timed step, L2 flushed first"}
+                "cold": {"us_per_launch": round(comb_cold_s * 1e6, 2), "achieved": round(cold_achieved, 1),
+                         "frac": round(cold_achieved / peak, 4),
+                         "phase_us": {"dispatch": round(d_cold * 1e3, 2), "receive_reply": round(r_cold * 1e3, 2),
+                                      "collect": round(c_cold * 1e3, 2)},
+                         "dispatch_phase_frac": round(d_cold_gbs / peak, 4),
+                         "note": "each phase's graph replayed alone with L2 flushed before it: the "
+                                 "combine finds none of the replies in L2"},
+                "note": "us_per_launch/frac: the per-phase graphs replayed one after another after "
+                        "each timed step, L2 flushed before the first (dispatch) phase only, as in "
+                        "the round trip: the combine finds the part of the scatter's rows that is "
+                        "still in L2"}
 
     # end to end through the public API, host buffers, copies inside the region
     e2e = None
@@ -742,44 +826,49 @@ def main():
         if ws > 1:  # the slowest rank, as for the headline
             e2e["value"] = round(reduce_max(e2e["value"], dev), 2)
 
-    sweep = None
+    sweep = under_load = None
     if not args.no_sweep and rank == 0:
-        sweep = measure_sweep(torch, afd, W, args.config, dev, flush)
+        sweep = measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=not args.no_cpu_baseline)
+        under_load = {"rows": measure_under_load(torch, afd, W, dev),
+                      "note": "100 replays of the exchange (one CUDA graph each) and 100 BF16 "
+                              "2048^3 GEMMs (torch.matmul) on a side stream, alone and together; "
+                              "num_sms caps the exchange's kernels"}
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and ws == 1:  # the oracle runs at N = 1 only
         times = cpu_oracle_round_trip_us(wl, inp, args.cpu_seconds, combine_mode=args.combine_mode)
         cpu = {"value": round(statistics.median(times), 1), "unit": "us", "cores": 1, "kind": "oracle",
                "sample": f"{len(times)} full round trips of the same workload "
-                         f"(validate, layout, dispatch, combine; identity expert), single-threaded C",
+                         f"(validate, layout, dispatch, combine; the expert stand-in untimed), "
+                         f"single-threaded C",
                "host": host_cpu()}
 
     buf.close()
     if rank == 0:
-        ctx = PAGES_CONTEXT_US.get((args.config, wl.H, wl.T[0]))
         line = {
             "metric": METRIC, "value": round(us, 2), "unit": "us", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic", "config": workload_config(wl, combine=args.combine_mode),
+            "execution": "one CUDA graph per round trip", "l2": L2_NOTE,
             "gbs": round(ab["total"] / (us * 1e-6) / 1e9, 1),
             "hbm_frac_of_peak": round(ab["total"] / (us * 1e-6) / 1e9 / peak, 4),
             "peak_gbs": peak, "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": (3 * launches_per_step - (wl.A - 1 if wl.F > 1 else 0)) * args.steps,
-            "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase, "
-                                 "and the round trip with one batched collect",
+            "gpu_launches": (4 * launches_per_step - (wl.A - 1 if wl.F > 1 else 0)) * args.steps,
+            "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase "
+                                 "(one after another, then each after an L2 flush), and the round "
+                                 "trip with one batched collect",
             "back_to_back_us": round(btb_us, 2),
             "eager_us": round(eager_us, 2),
             "collect_all_us": round(batched_us, 2),
             "collect_all_note": "the same round trip with afd_source_collect_all (one combine "
                                 "launch for every source) in place of one collect per source",
             "wall_s": round(wall, 3),
-            "context": ({"pages_4xH100_nvlink_us": ctx,
-                         "note": "multi-GPU communication-only figure from the pages; not this workload"}
-                        if ctx else None),
+            "context": pages_context(args.config, wl.T[0], args.combine_mode),
             "sweep": sweep,
+            "under_load": under_load,
             "native_digest": native_digest(),
         }
         print(json.dumps(line))
@@ -882,82 +971,6 @@ def measure_e2e(torch, buf, wl, inp, dev, steps: int, flush):
                     "pinned buffers passed to the calls, which read and write them over the "
                     "host link. *_us = the step captured once as a CUDA graph and replayed, "
                     "*_eager_us = issued call by call; value = the faster method"}
-
-
-def measure_sweep(torch, afd, W, config, dev, flush):
-    """Graph-replayed round trip at the workload's other token counts, with a
-    full dispatch, with a cached dispatch (the last exchange's routing
-    reused), and with a full dispatch and one batched collect. Each is timed
-    with L2 flushed before every replay, and replayed 50 times back to back
-    (small batches then stay in L2, as they would between decode steps)."""
-    out = {}
-    table = {"2A2F": (1, 8, 32, 128, 512, 2048), "2A2F-H4096": (1, 128, 2048)}
-    for name, Ts in (("2A2F", table["2A2F"]), ("2A2F-H4096", table["2A2F-H4096"])):
-        for T in Ts:
-            wl = W.named(name, T=T)
-            inp = W.make_inputs(wl)
-            buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha)
-            xs = [torch.from_numpy(inp.x[s, :T].view(np.int16).copy()).to(dev).view(torch.bfloat16)
-                  for s in range(wl.A)]
-            ids = [torch.from_numpy(inp.ids[s, :T].copy()).to(dev) for s in range(wl.A)]
-            ws_ = [torch.from_numpy(inp.w[s, :T].copy()).to(dev) for s in range(wl.A)]
-            outs = [torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev) for _ in range(wl.A)]
-
-            def exchange():
-                for s in range(wl.A):
-                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
-                for f in range(wl.F):
-                    r = buf.worker_receive(f, bucket=wl.bucket)
-                    buf.worker_reply(f, r.rows, r.receipt)
-                for s in range(wl.A):
-                    buf.source_collect(s, out=outs[s])
-
-            def exchange_cached():
-                for s in range(wl.A):
-                    buf.source_dispatch_cached(s, xs[s], ws_[s], bucket=wl.bucket)
-                for f in range(wl.F):
-                    r = buf.worker_receive(f, bucket=wl.bucket)
-                    buf.worker_reply(f, r.rows, r.receipt)
-                for s in range(wl.A):
-                    buf.source_collect(s, out=outs[s])
-
-            def exchange_batched():
-                for s in range(wl.A):
-                    buf.source_dispatch(s, xs[s], ids[s], ws_[s], bucket=wl.bucket)
-                for f in range(wl.F):
-                    r = buf.worker_receive(f, bucket=wl.bucket)
-                    buf.worker_reply(f, r.rows, r.receipt)
-                buf.source_collect_all(outs=outs)
-
-            for label, fn in (("", exchange), (" cached", exchange_cached),
-                              (" batched collect", exchange_batched)):
-                fn()
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    fn()
-                for _ in range(3):
-                    g.replay()
-                times = []
-                for _ in range(10):
-                    flush()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    g.replay()
-                    b.record()
-                    b.synchronize()
-                    times.append(a.elapsed_time(b) * 1e3)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                for _ in range(50):
-                    g.replay()
-                b.record()
-                b.synchronize()
-                del g
-                out[f"{name} T={T}{label}"] = round(statistics.median(times), 2)
-                out[f"{name} T={T}{label} back to back"] = round(a.elapsed_time(b) * 1e3 / 50, 2)
-            buf.close()
-    return out
 
 
 if __name__ == "__main__":

@@ -87,3 +87,39 @@ def test_reference_arm_reports_the_combine_mode(mode):
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["config"]["combine"] == mode
     assert line["value"] > 0 and line["cpu_baseline"]["cores"] == 1
+
+
+def test_pages_context_cells():
+    """The pages' "Result" cells attached to sweep rows: the layout, hidden
+    size and dtype must match, and only the pages' token counts have one."""
+    import bench
+
+    c = bench.pages_context("2A2F", 1)
+    assert (c["afdEP_comm_us"], c["fastafd_m2n_us"]) == (20.7, 31.7)
+    assert bench.pages_context("2A2F-H4096", 2048)["afdEP_comm_us"] == 383.2
+    assert bench.pages_context("skew-3A1F", 512)["afdEP_comm_us"] == 109.4
+    assert bench.pages_context("skew-1A3F", 32)["fastafd_m2n_us"] == 32.8
+    assert bench.pages_context("fp8-2A2F", 128)["afdEP_comm_us"] == 34.5
+    assert bench.pages_context("fp8-2A1F", 128) is None      # no such layout on the pages
+    assert bench.pages_context("2A2F", 16) is None            # no such token count
+    assert bench.pages_context("tiny", 16) is None
+    for name, Ts, _ in bench.SWEEP:                          # every row's T is a workload's own
+        assert all(T >= 1 for T in Ts)
+
+
+def test_reference_arm_config_equals_ours_and_runs_fp8():
+    """Both arms describe the workload with the same config dict; the
+    reference arm also times the FP8 round trip (its expert stand-in untimed)."""
+    import json
+
+    import bench
+    from combine_attention_ffn_gb300 import workloads as W
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "fp8-2A2F", "--tokens", "1", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    wl = W.named("fp8-2A2F", T=1)
+    assert line["config"] == bench.workload_config(wl)
+    assert line["dtype"] == "fp8" and line["value"] > 0
