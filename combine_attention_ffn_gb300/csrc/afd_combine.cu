@@ -40,6 +40,49 @@ constexpr int kGroup = 8;  // routes whose loads are issued together
 // Resident blocks per SM of combine_kernel<1> (set by configure_combine_kernels).
 int g_seg1_blocks_per_sm = 0;
 
+// Reply rows: 16-byte non-coherent loads that skip L1 allocation (the
+// texture path streams this gather much faster than L2-only loads). Route
+// receipts: L2-only loads.
+//
+// A combine launched right after the previous combine of the same exchange
+// on the same stream (p.early) needs no dependency wait to start: its launch
+// implies that every block of that combine has passed its own wait (it lets
+// dependents launch only after it), so the scatter, the expert and
+// everything before them have completed, and the replies stay unchanged for
+// this kernel's whole lifetime, which is what non-coherent loads require. It
+// waits at its end instead, so that it completes only after its predecessor
+// (what comes after it in the stream may rely on the whole exchange being
+// done). Any other combine waits first and then lets dependents launch.
+__device__ __forceinline__ uint4 ld_reply(const uint4* p, bool early) {
+#if AFD_EARLY_LOADS == 1
+  if (early) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+  }
+#endif
+  (void)early;
+  return ld_once(p);
+}
+
+__device__ __forceinline__ void combine_begin(const CombineParams& p) {
+  if (!p.early) {
+    pdl_wait();
+  } else {
+#if AFD_EARLY_FENCE
+    // a device-scope acquire before the first load: no line an earlier
+    // kernel left in this SM's L1 is used
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+#endif
+  }
+  pdl_launch_dependents();
+}
+__device__ __forceinline__ void combine_end(const CombineParams& p) {
+  if (p.early) pdl_wait();
+}
+
 __device__ __forceinline__ int source_of(const CombineParams& p, int gt) {
   int s = 0;
   while (s + 1 < p.A && gt >= p.tok_off[s + 1]) ++s;
@@ -62,8 +105,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int U>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
-  pdl_launch_dependents();
-  pdl_wait();  // receipts and replies come from earlier kernels
+  combine_begin(p);  // receipts and replies come from earlier kernels
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -77,7 +119,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     const int s = source_of(p, gt);
     const int t = gt - p.tok_off[s];
     int2 r = make_int2(-1, 0);
-    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    if (lane < K) r = __ldcg(p.routes[s] + (int64_t)t * K + lane);
     const int v0 = seg * 32 * U + lane;
 
     float acc[U][8];
@@ -100,7 +142,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
           const uint4* row = reinterpret_cast<const uint4*>(
               p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H);
 #pragma unroll
-          for (int u = 0; u < U; ++u) buf[j][u] = ld_once(row + v0 + u * 32);
+          for (int u = 0; u < U; ++u) buf[j][u] = ld_reply(row + v0 + u * 32, p.early);
         }
       }
 #pragma unroll
@@ -122,6 +164,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
       out_row[v0 + u * 32] = o;
     }
   }
+  combine_end(p);
 }
 
 // ---- two-stage combine (optionally with E4M3 partials) ----
@@ -182,10 +225,10 @@ __device__ __forceinline__ uint32_t token_routes(const CombineParams& p, int2 r,
 }
 
 __device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* const (&rowp)[kGroup],
-                                         uint32_t okmask, int v) {
+                                         uint32_t okmask, int v, bool early) {
 #pragma unroll
   for (int j = 0; j < kGroup; ++j)
-    if ((okmask >> j) & 1u) buf[j] = ld_once(reinterpret_cast<const uint4*>(rowp[j]) + v);
+    if ((okmask >> j) & 1u) buf[j] = ld_reply(reinterpret_cast<const uint4*>(rowp[j]) + v, early);
 }
 
 // Sums one segment (this lane's 8 elements of every route) and stores it.
@@ -252,8 +295,7 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
 
 template <int kMode>
 __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_STAGE_BLOCKS) combine_token_kernel(const __grid_constant__ CombineParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
+  combine_begin(p);
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -270,7 +312,7 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_S
     const int s = source_of(p, gt);
     const int t = gt - p.tok_off[s];
     int2 r = make_int2(-1, 0);
-    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    if (lane < K) r = __ldcg(p.routes[s] + (int64_t)t * K + lane);
     const uint16_t* rowp[kGroup];
     float wk[kGroup];
     int wf[kGroup];
@@ -279,24 +321,24 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_S
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
     uint4 a[kGroup], b[kGroup];
-    load_seg(a, rowp, okmask, lane);
+    load_seg(a, rowp, okmask, lane, p.early);
     int seg = 0;
     for (; seg + 2 <= nseg; seg += 2) {
-      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane);
+      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane, p.early);
       sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
-      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane);
+      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane, p.early);
       sum_seg<kMode>(out_row, b, wk, wf, okmask, (seg + 1) * 32 + lane);
     }
     if (seg < nseg) sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
   }
+  combine_end(p);
 }
 
 // Few tokens: a warp per (token, 512-byte segment), as combine_kernel<1>,
 // with the two-stage rule.
 template <int kMode>
 __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_constant__ CombineParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
+  combine_begin(p);
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -310,16 +352,17 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
     const int s = source_of(p, gt);
     const int t = gt - p.tok_off[s];
     int2 r = make_int2(-1, 0);
-    if (lane < K) r = p.routes[s][(int64_t)t * K + lane];
+    if (lane < K) r = __ldcg(p.routes[s] + (int64_t)t * K + lane);
     const uint16_t* rowp[kGroup];
     float wk[kGroup];
     int wf[kGroup];
     const uint32_t okmask = token_routes(p, r, rowp, wk, wf);
     uint4 buf[kGroup];
-    load_seg(buf, rowp, okmask, seg * 32 + lane);
+    load_seg(buf, rowp, okmask, seg * 32 + lane, p.early);
     sum_seg<kMode>(reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]), buf, wk, wf,
                    okmask, seg * 32 + lane);
   }
+  combine_end(p);
 }
 
 __global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {

@@ -39,6 +39,15 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_TWO_STAGE_BLOCKS
 #define AFD_TWO_STAGE_BLOCKS 7    // resident two-warp blocks per SM asked of the two-stage per-token combine
 #endif
+#ifndef AFD_EARLY_LOADS
+#define AFD_EARLY_LOADS 0         // 1: an early-started combine reads replies with ld.global.cg (L2 only)
+#endif
+#ifndef AFD_EARLY_FENCE
+#define AFD_EARLY_FENCE 1         // an early-started combine begins with a device-scope acquire fence
+#endif
+#ifndef AFD_COMBINE_EARLY
+#define AFD_COMBINE_EARLY 1       // a combine right after another one of the same exchange starts at once
+#endif
 #ifndef AFD_TOKEN_COMBINE_MIN
 #define AFD_TOKEN_COMBINE_MIN 4  // x SMs: tokens from which the per-token combine is used
 #endif
@@ -111,6 +120,8 @@ struct CombineParams {
   const uint16_t* reply[kMaxWorkers];// BF16 [rows][H] per worker
   int32_t A, K, H, total_tokens;
   int32_t mode;                      // AFD_COMBINE_*
+  int32_t early;                     // 1: the previous kernel on the stream is a combine of the
+                                     // same exchange (start at once, wait for it at the end)
 };
 
 struct CopyParams {

@@ -72,6 +72,11 @@ struct afd_ctx {
   int bucket;
   int rhc;
   bool cached;          // this exchange reuses the last layout
+  // the last call of this exchange launched a combine on combine_stream (the
+  // next combine on that stream may start without the dependency wait)
+  bool combine_last;
+  cudaStream_t combine_stream;
+  bool combine_captured;
   // the last layout that a dispatch computed (what a cached dispatch reuses)
   bool layout_valid;
   int layout_bucket;
@@ -207,6 +212,9 @@ int64_t recv_rows_for(const afd_ctx* c, int64_t bucket) {
 void reset_exchange(afd_ctx* c) {
   c->phase = kIdle;
   c->cached = false;
+  c->combine_last = false;
+  c->combine_stream = nullptr;
+  c->combine_captured = false;
   c->staged_n = c->replied_n = c->collected_n = 0;
   c->bucket = -1;
   c->rhc = -1;
@@ -728,6 +736,11 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
   } else if (T > 0) {
     CombineParams p;
     memset(&p, 0, sizeof p);
+    // Started at once when the previous call was a collect of this exchange
+    // that launched a combine on the same stream (and capture state): the
+    // stream then holds nothing between the two combines but host-side marks.
+    p.early = AFD_COMBINE_EARLY && c->combine_last && c->combine_stream == stream &&
+              c->combine_captured == is_capturing(stream);
     p.routes[0] = c->routes + (int64_t)c->src[source].tok_off * g.top_k;
     p.out[0] = static_cast<uint16_t*>(out);
     p.out_stride[0] = g.hidden;
@@ -741,6 +754,9 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
     cudaError_t e = afd::launch_combine(p, c->sm_cap, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
   }
+  c->combine_last = g.num_workers > 1 && T > 0;
+  c->combine_stream = stream;
+  c->combine_captured = is_capturing(stream);
   if (view_out) {
     view_out->data = as_view ? static_cast<const void*>(inbox) : static_cast<const void*>(user_out);
     view_out->row_stride = g.hidden;
@@ -858,6 +874,7 @@ afd_status afd_clear_error(afd_ctx* c, afd_stream stream_) {
   if (st != AFD_OK) return st;
   cudaError_t e = cudaMemsetAsync(c->err, 0xff, sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "clearing the route error");
+  c->combine_last = false;  // the next combine waits for the work before it
   return mark_stream(c, stream);
 }
 
