@@ -408,9 +408,11 @@ class Rig:
         self.buf.close()
 
 
-def replay_stats(torch, g, flush, n_flushed: int = 10, n_btb: int = 50):
-    """Median µs of one replay with L2 flushed before it (outside its events),
-    and mean µs of n_btb replays back to back."""
+def replay_stats(torch, g, flush, n_flushed: int = 20, n_btb: int = 50):
+    """Mean µs of one replay with L2 flushed before it (outside its events),
+    and mean µs of n_btb replays back to back. Event timestamps fall on a
+    grid of about 2 µs on this hardware, so a median of single replays sits
+    on a grid point; the mean of many resolves finer."""
     for _ in range(3):
         g.replay()
     times = []
@@ -428,7 +430,7 @@ def replay_stats(torch, g, flush, n_flushed: int = 10, n_btb: int = 50):
         g.replay()
     b.record()
     b.synchronize()
-    return statistics.median(times), a.elapsed_time(b) * 1e3 / n_btb
+    return statistics.mean(times), a.elapsed_time(b) * 1e3 / n_btb
 
 
 # Rows of the default run: every workload at the token counts of its
@@ -441,8 +443,8 @@ SWEEP = (("tiny", (16,), "fused"), ("2A2F", (1, 8, 32, 128, 512, 2048), "fused")
 
 
 def measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=True):
-    """Every row of SWEEP, one CUDA graph replay per round trip: µs after an
-    L2 flush and back to back, algorithmic bytes, GB/s and the fraction of
+    """Every row of SWEEP, one CUDA graph replay per round trip: mean µs after
+    an L2 flush and back to back, algorithmic bytes, GB/s and the fraction of
     the HBM peak (from 512 tokens per source; below, the round trip is bound
     by latency), the pages' cell for the same layout as context, and the
     oracle's time for the same round trip on this host. Single-worker
