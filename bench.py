@@ -625,7 +625,17 @@ def main():
         torch.distributed.barrier()
     wl = W.named(args.config, T=args.tokens)
     if wl.dtype == "fp8":
-        raise SystemExit("the headline times the BF16 identity-expert round trip; FP8 rows are in the sweep")
+        if not args.profile_exchanges:
+            raise SystemExit("the headline times the BF16 identity-expert round trip; FP8 rows are in the sweep")
+        # an untimed program for an external profiler: the sweep's FP8 exchange
+        # (its replies computed once by the stand-in expert), repeated
+        rig = Rig(torch, afd, W, args.config, args.tokens, dev, combine=args.combine_mode)
+        for _ in range(args.profile_exchanges):
+            rig.exchange()
+        torch.cuda.synchronize()
+        rig.close()
+        print(f"ran {args.profile_exchanges} exchanges of {wl.name} T={wl.T[0]}")
+        return 0
     inp = W.make_inputs(wl)
     buf = afd.Buffer(wl.A, wl.F, wl.E, wl.K, wl.H, wl.capacity, wl.alpha, wl.dtype,
                      combine_mode=COMBINE_MODES[args.combine_mode])
