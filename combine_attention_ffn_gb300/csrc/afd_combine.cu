@@ -37,8 +37,9 @@ namespace {
 
 constexpr int kGroup = 8;  // routes whose loads are issued together
 
-// Resident blocks per SM of combine_kernel<1> (set by configure_combine_kernels).
+// Resident blocks per SM of combine_kernel<1> and <2> (set by configure_combine_kernels).
 int g_seg1_blocks_per_sm = 0;
+int g_seg2_blocks_per_sm = 0;
 
 // Reply rows: 16-byte non-coherent loads that skip L1 allocation (the
 // texture path streams this gather much faster than L2-only loads). Route
@@ -421,12 +422,28 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
                : launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>, grid, 256, stream, p);
   }
   const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
-  const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
   // Two slices per item when one slice per warp would need more warps than
   // the SMs hold at once: every warp then still has exactly one item, in a
   // single wave, instead of a second wave paying the whole latency again.
   const int64_t resident1 = (int64_t)sm_cap * (g_seg1_blocks_per_sm > 0 ? g_seg1_blocks_per_sm : 1) * 8;
   const bool wide = (p.H % 512 == 0) && slices > resident1;
+  if (AFD_COMBINE_SHARE && p.share > 1 && p.H % 512 == 0) {
+    // One combine per source, each started while the one before it runs
+    // (early start). When their blocks could not all be resident at once,
+    // every launch gets an equal share of the SMs instead (two slices per
+    // item, a few items per warp), so that they run side by side rather than
+    // each waiting for the previous one's blocks to leave.
+    const int64_t need = ((wide ? slices / 2 : slices) + 7) / 8;
+    const int bps0 = wide ? g_seg2_blocks_per_sm : g_seg1_blocks_per_sm;
+    if (need * p.share > (int64_t)sm_cap * (bps0 > 0 ? bps0 : 1)) {
+      int64_t grid = (int64_t)sm_cap * (g_seg2_blocks_per_sm > 0 ? g_seg2_blocks_per_sm : 1) / p.share;
+      const int64_t need2 = (slices / 2 + 7) / 8;
+      if (grid > need2) grid = need2;
+      if (grid < 1) grid = 1;
+      return launch_pdl(combine_kernel<2>, grid, 256, stream, p);
+    }
+  }
+  const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
   const int64_t items = wide ? slices / 2 : slices;
   int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;
@@ -446,6 +463,7 @@ cudaError_t configure_combine_kernels() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg1_blocks_per_sm, combine_kernel<1>, 256, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg2_blocks_per_sm, combine_kernel<2>, 256, 0);
   return e;
 }
 

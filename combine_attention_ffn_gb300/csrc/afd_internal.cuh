@@ -48,6 +48,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_COMBINE_EARLY
 #define AFD_COMBINE_EARLY 1       // a combine right after another one of the same exchange starts at once
 #endif
+#ifndef AFD_COMBINE_SHARE
+#define AFD_COMBINE_SHARE 1       // per-source segmented combines take an equal share of the SMs
+#endif
 #ifndef AFD_TOKEN_COMBINE_MIN
 #define AFD_TOKEN_COMBINE_MIN 4  // x SMs: tokens from which the per-token combine is used
 #endif
@@ -122,6 +125,8 @@ struct CombineParams {
   int32_t mode;                      // AFD_COMBINE_*
   int32_t early;                     // 1: the previous kernel on the stream is a combine of the
                                      // same exchange (start at once, wait for it at the end)
+  int32_t share;                     // combines of this exchange expected to run side by side
+                                     // (one per source when each source collects on its own)
 };
 
 struct CopyParams {

@@ -741,6 +741,7 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
     // stream then holds nothing between the two combines but host-side marks.
     p.early = AFD_COMBINE_EARLY && c->combine_last && c->combine_stream == stream &&
               c->combine_captured == is_capturing(stream);
+    p.share = g.num_sources;  // each source collects on its own
     p.routes[0] = c->routes + (int64_t)c->src[source].tok_off * g.top_k;
     p.out[0] = static_cast<uint16_t*>(out);
     p.out_stride[0] = g.hidden;
