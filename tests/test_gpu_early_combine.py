@@ -77,3 +77,43 @@ def test_early_combine_sees_every_new_reply(name, T):
         del g
     finally:
         buf.close()
+
+
+@pytest.mark.parametrize("order", [(0, 1, 2), (2, 0, 1)])
+def test_three_sources_collected_one_by_one(order):
+    """Three sources, two workers: each later collect starts its combine
+    early; with ragged mid-size batches every per-source launch takes a third
+    of the SMs. Any collect order, call by call and from a graph."""
+    wl = W.Workload("3A2F-ragged", A=3, F=2, E=64, K=6, H=2048, alpha=16, capacity=512, bucket=512,
+                    T=(300, 512, 417), seed=717)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE)
+    buf = GH.make_buffer(wl)
+    try:
+        dev = GH.to_device(inp)
+        outs = GH.alloc_outs(wl)
+
+        def exchange():
+            for s in range(wl.A):
+                buf.source_dispatch(s, dev.x[s], dev.ids[s], dev.w[s], bucket=wl.bucket)
+            recvs = {f: buf.worker_receive(f, bucket=wl.bucket) for f in range(wl.F)}
+            replies = {f: GH.expert_reply(wl, f, recvs[f], GH.SCALE) for f in range(wl.F)}
+            for f in range(wl.F):
+                buf.worker_reply(f, replies[f], recvs[f].receipt)
+            for s in order:
+                buf.source_collect(s, out=outs[s])
+
+        exchange()
+        torch.cuda.synchronize()
+        GH.check_outputs(wl, outs, exp)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            exchange()
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        GH.check_outputs(wl, outs, exp)
+        del g
+    finally:
+        buf.close()
