@@ -90,7 +90,7 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
-def algorithmic_bytes(wl, inp, view: bool = False) -> dict:
+def algorithmic_bytes(wl, inp) -> dict:
     """Bytes the exchange must move once (read x, write routed rows, read
     replies, write out) plus its metadata, per phase and per launch."""
     valid = 0
@@ -101,10 +101,8 @@ def algorithmic_bytes(wl, inp, view: bool = False) -> dict:
     R_in = wl.row_bytes + (4 * (H // 128) if wl.dtype == "fp8" else 0)
     dispatch = toks * R_in + valid * R_in + toks * K * (8 + 4) + valid * (4 + 4) + toks * K * (4 + 8)
     combine = valid * 2 * H + toks * 2 * H + toks * K * 8
-    # one worker without the view: collect copies the inbox into `out`
-    copy = 2 * toks * 2 * H if (wl.F == 1 and not view) else 0
-    return dict(valid=valid, dispatch=dispatch, combine=combine, copy=copy,
-                total=dispatch + combine + copy,
+    return dict(valid=valid, dispatch=dispatch, combine=combine,
+                total=dispatch + combine,
                 payload=toks * R_in + valid * R_in + valid * 2 * H + toks * 2 * H)
 
 
@@ -464,7 +462,7 @@ def measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=True):
                 g = rig.graph(**kw)
                 us, btb = replay_stats(torch, g, flush)
                 del g
-                ab = algorithmic_bytes(wl, inp, view=kw.get("view", False))
+                ab = algorithmic_bytes(wl, inp)
                 gbs = ab["total"] / (us * 1e-6) / 1e9
                 row = {"config": name, "T": T, "combine": mode, "variant": label, "us": round(us, 2),
                        "us_back_to_back": round(btb, 2), "bytes": int(ab["total"]), "gbs": round(gbs, 1),
@@ -602,7 +600,7 @@ def main():
 
     import torch
 
-    # the receive/reply phase graph holds no kernel when F > 1 (only host checks)
+    # the receive/reply phase graph holds no kernel (only host checks)
     warnings.filterwarnings("ignore", message="The CUDA Graph is empty")
     ws, rank, local = dist_env()
     if ws > 1:
@@ -787,16 +785,14 @@ def main():
     ab = algorithmic_bytes(wl, inp)
     peak, peak_kind = load_peaks()
     us = ms * 1e3
-    launches_per_step = (1 if buf_small else 2) + (wl.A if wl.F > 1 else 1 + wl.A)
+    launches_per_step = (1 if buf_small else 2) + wl.A
 
     # dominant kernel: the combine has the largest share of the launch list
-    # (profiles/launches_*.md); one launch per source for F > 1, one for all
-    # sources for F = 1. The dispatch phase (layout + scatter) is reported too.
-    # F = 1 combines at reply (its collect is a view or a copy); F > 1 combines
-    # at collect, and its receive/reply graph launches no kernel at all
-    comb_ms = r_ms if wl.F == 1 else c_ms
-    n_launch = wl.A if wl.F > 1 else 1
-    per_launch_s = comb_ms / n_launch * 1e-3
+    # (profiles/launches_*.md), one launch per source, all in the collect
+    # phase; the receive/reply phase launches no kernel at all. The dispatch
+    # phase (layout + scatter) is reported too.
+    n_launch = wl.A
+    per_launch_s = c_ms / n_launch * 1e-3
     per_launch_bytes = ab["combine"] / n_launch
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     kname = "combine_token_kernel" if sum(wl.T) // n_launch >= 4 * n_sms else (
@@ -806,7 +802,7 @@ def main():
     achieved = per_launch_bytes / per_launch_s / 1e9
     traffic = kernel_traffic("combine", f"{wl.name}-T{wl.T[0]}") if args.combine_mode == "fused" else None
     d_gbs = ab["dispatch"] / (d_ms * 1e-3) / 1e9
-    comb_cold_s = (r_cold if wl.F == 1 else c_cold) / n_launch * 1e-3
+    comb_cold_s = c_cold / n_launch * 1e-3
     cold_achieved = per_launch_bytes / comb_cold_s / 1e9
     d_cold_gbs = ab["dispatch"] / (d_cold * 1e-3) / 1e9
     roofline = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
@@ -868,7 +864,7 @@ def main():
             "peak_gbs": peak, "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": (4 * launches_per_step - (wl.A - 1 if wl.F > 1 else 0)) * args.steps,
+            "gpu_launches": (4 * launches_per_step - (wl.A - 1)) * args.steps,
             "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase "
                                  "(one after another, then each after an L2 flush), and the round "
                                  "trip with one batched collect",

@@ -321,7 +321,7 @@ class Buffer:
         return out
 
     def source_collect_all(self, *, view: bool = False, outs=None, num_tokens=None, stream=None):
-        """Every source's result with one call (one combine launch when F > 1).
+        """Every source's result with one call (one combine launch).
         Returns a list of BF16 [T_s, H] tensors (views with view=True and F == 1)."""
         if outs is None:
             if view and self.F == 1:

@@ -1,5 +1,5 @@
-// Combine kernel: gathers each token's reply rows and sums them with the
-// routing weights; and the collect copy kernel.
+// Combine kernels: gather each token's reply rows and sum them with the
+// routing weights.
 //
 // What it computes follows the afdEP-comm "API contract" (source_collect:
 // BF16 [T,H] summed over the selected experts in the source's token order,
@@ -366,21 +366,6 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
   combine_end(p);
 }
 
-__global__ void __launch_bounds__(256) copy_kernel(const __grid_constant__ CopyParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int nvec = p.H >> 3;
-  const int64_t total = (int64_t)p.rows * nvec;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t row = i / nvec;
-    const int v = (int)(i % nvec);
-    const uint4* src = reinterpret_cast<const uint4*>(p.src + row * p.src_stride);
-    uint4* dst = reinterpret_cast<uint4*>(p.dst + row * p.dst_stride);
-    dst[v] = ld_once(src + v);
-  }
-}
-
 template <typename Kernel, typename Params>
 cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stream, const Params& p) {
   cudaLaunchConfig_t cfg = {};
@@ -458,22 +443,12 @@ cudaError_t configure_combine_kernels() {
                         (const void*)combine_token_kernel<AFD_COMBINE_TWO_STAGE_FP8>,
                         (const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
                         (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>,
-                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>,
-                        (const void*)copy_kernel})
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg1_blocks_per_sm, combine_kernel<1>, 256, 0);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg2_blocks_per_sm, combine_kernel<2>, 256, 0);
   return e;
-}
-
-cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream) {
-  const int64_t total = (int64_t)p.rows * (p.H >> 3);
-  if (total <= 0) return cudaSuccess;
-  int64_t grid = (total + 255) / 256;
-  const int64_t cap = (int64_t)sm_cap * 8;
-  if (grid > cap) grid = cap;
-  return launch_pdl(copy_kernel, grid, 256, stream, p);
 }
 
 }  // namespace afd

@@ -129,12 +129,6 @@ struct CombineParams {
                                      // (one per source when each source collects on its own)
 };
 
-struct CopyParams {
-  const uint16_t* src;
-  uint16_t* dst;
-  int64_t src_stride, dst_stride;  // elements
-  int32_t rows, H;
-};
 
 // Launchers (return the launch's cudaError_t).
 bool dispatch_is_small(const DispatchParams& p);
@@ -142,7 +136,6 @@ int layout_ctas_for(int total_tokens, int sm_cap, int max_ctas);
 cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
-cudaError_t launch_copy(const CopyParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t configure_dispatch_kernels(int* max_ctas);
 cudaError_t configure_combine_kernels();
 

@@ -21,7 +21,6 @@
 #include "afd_internal.cuh"
 
 using afd::CombineParams;
-using afd::CopyParams;
 using afd::DispatchParams;
 using afd::SourceDesc;
 
@@ -669,31 +668,7 @@ afd_status afd_worker_reply(afd_ctx* c, int32_t worker, const void* rows, int64_
   c->reply[worker] = static_cast<const uint16_t*>(rows);
   c->replied[worker] = true;
   c->replied_n += 1;
-  if (c->replied_n == g.num_workers) {
-    if (g.num_workers == 1) {
-      // Single worker: every top-k row is local, so the combine of every
-      // source runs now, into the context's inboxes.
-      CombineParams p;
-      memset(&p, 0, sizeof p);
-      int tok = 0;
-      for (int s = 0; s < g.num_sources; ++s) {
-        p.routes[s] = c->routes + (int64_t)c->src[s].tok_off * g.top_k;
-        p.out[s] = c->inbox + (int64_t)s * g.capacity * g.hidden;
-        p.out_stride[s] = g.hidden;
-        p.tok_off[s] = tok;
-        tok += c->src[s].T;
-      }
-      p.reply[0] = c->reply[0];
-      p.mode = g.combine_mode;
-      p.A = g.num_sources;
-      p.K = g.top_k;
-      p.H = g.hidden;
-      p.total_tokens = tok;
-      cudaError_t e = afd::launch_combine(p, c->sm_cap, stream);
-      if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
-    }
-    c->phase = kReplied;
-  }
+  if (c->replied_n == g.num_workers) c->phase = kReplied;
   return mark_stream(c, stream);
 }
 
@@ -720,20 +695,8 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
   afd_status st = order_stream(c, stream);
   if (st != AFD_OK) return st;
 
-  const uint16_t* inbox = c->inbox ? c->inbox + (int64_t)source * g.capacity * g.hidden : nullptr;
-  if (g.num_workers == 1) {
-    if (!as_view && T > 0) {
-      CopyParams p;
-      p.src = inbox;
-      p.dst = static_cast<uint16_t*>(out);
-      p.src_stride = g.hidden;
-      p.dst_stride = g.hidden;
-      p.rows = T;
-      p.H = g.hidden;
-      cudaError_t e = afd::launch_copy(p, c->sm_cap, stream);
-      if (e != cudaSuccess) return cuda_fail(c, e, "copy launch");
-    }
-  } else if (T > 0) {
+  uint16_t* inbox = c->inbox ? c->inbox + (int64_t)source * g.capacity * g.hidden : nullptr;
+  if (T > 0) {
     CombineParams p;
     memset(&p, 0, sizeof p);
     // Started at once when the previous call was a collect of this exchange
@@ -743,7 +706,7 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
               c->combine_captured == is_capturing(stream);
     p.share = g.num_sources;  // each source collects on its own
     p.routes[0] = c->routes + (int64_t)c->src[source].tok_off * g.top_k;
-    p.out[0] = static_cast<uint16_t*>(out);
+    p.out[0] = as_view ? inbox : static_cast<uint16_t*>(out);
     p.out_stride[0] = g.hidden;
     p.tok_off[0] = 0;
     for (int f = 0; f < g.num_workers; ++f) p.reply[f] = c->reply[f];
@@ -755,7 +718,7 @@ afd_status afd_source_collect(afd_ctx* c, int32_t source, void* out, int32_t vie
     cudaError_t e = afd::launch_combine(p, c->sm_cap, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
   }
-  c->combine_last = g.num_workers > 1 && T > 0;
+  c->combine_last = T > 0;
   c->combine_stream = stream;
   c->combine_captured = is_capturing(stream);
   if (view_out) {
@@ -779,30 +742,16 @@ afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, a
   const afd_config& g = c->cfg;
   if (c->phase != kReplied) return fail(c, AFD_ERR_STATE, "replies are not complete");
   if (c->collected_n != 0) return fail(c, AFD_ERR_STATE, "some sources are already collected");
-  if (!outs && !(view && g.num_workers == 1)) return fail(c, AFD_ERR_ARG, "outs is required");
-  if (g.num_workers == 1) {
-    // copies or views, source by source (no combine runs at collect)
-    for (int s = 0; s < g.num_sources; ++s) {
-      const bool as_view = view && g.num_workers == 1;
-      if (!as_view && c->src[s].T > 0) {
-        void* d = nullptr;
-        if (!outs[s]) return fail(c, AFD_ERR_ARG, "outs[%d] is required", s);
-        afd_status r = resolve(c, outs[s], "outs[s]", &d);
-        if (r != AFD_OK) return r;
-        if (!aligned16(d)) return fail(c, AFD_ERR_ARG, "outs[%d] must be 16-byte aligned", s);
-      }
-    }
-    for (int s = 0; s < g.num_sources; ++s) {
-      afd_status st = afd_source_collect(c, s, outs ? outs[s] : nullptr, view, stream_,
-                                         views ? views + s : nullptr);
-      if (st != AFD_OK) return st;
-    }
-    return AFD_OK;
-  }
+  const bool as_view = view && g.num_workers == 1;
+  if (!outs && !as_view) return fail(c, AFD_ERR_ARG, "outs is required");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   void* dout[afd::kMaxSources] = {};
   for (int s = 0; s < g.num_sources; ++s) {
     if (c->src[s].T == 0) continue;
+    if (as_view) {
+      dout[s] = c->inbox + (int64_t)s * g.capacity * g.hidden;
+      continue;
+    }
     if (!outs[s]) return fail(c, AFD_ERR_ARG, "outs[%d] is required", s);
     afd_status r = resolve(c, outs[s], "outs[s]", &dout[s]);
     if (r != AFD_OK) return r;
@@ -832,10 +781,10 @@ afd_status afd_source_collect_all(afd_ctx* c, void* const* outs, int32_t view, a
   if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
   for (int s = 0; s < g.num_sources; ++s) {
     if (views) {
-      views[s].data = outs[s];
+      views[s].data = as_view ? static_cast<const void*>(dout[s]) : static_cast<const void*>(outs[s]);
       views[s].row_stride = g.hidden;
       views[s].num_tokens = c->src[s].T;
-      views[s].is_view = 0;
+      views[s].is_view = as_view ? 1 : 0;
     }
   }
   reset_exchange(c);

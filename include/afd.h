@@ -221,11 +221,10 @@ AFD_API afd_status afd_worker_receive(afd_ctx* ctx, int32_t worker, int32_t buck
  *             the received rows themselves (an identity expert, BF16 only).
  *   num_rows  must equal the afd_recv.num_rows of this worker's receive
  *   receipt   must equal the afd_recv.receipt of this worker's receive
- * The library applies each routing weight exactly once, in the combine. With
- * F == 1, this call enqueues the combine of every source into the context's
- * inboxes (one worker holds all of a token's experts, as in "10. Single-FFN
- * reduction" of the afdEP-comm design page); with F > 1 the combine runs in
- * afd_source_collect.
+ * The library applies each routing weight exactly once, in the combine,
+ * which runs in afd_source_collect (one launch per source) or
+ * afd_source_collect_all (one launch for all sources), for every F. This call
+ * launches no kernel.
  * Errors: AFD_ERR_STATE, AFD_ERR_RECEIPT, AFD_ERR_ARG, AFD_ERR_CUDA. */
 AFD_API afd_status afd_worker_reply(afd_ctx* ctx, int32_t worker, const void* rows, int64_t num_rows,
                             uint64_t receipt, afd_stream stream);
@@ -245,11 +244,12 @@ typedef struct afd_view {
  * order. Counterpart of source_collect(*, view=False) in the "API contract".
  *   out   device BF16 [T, H] (contiguous), T = the source's num_tokens; may be
  *         NULL only when view = 1 and F == 1
- *   view  1 asks for the single-worker view: with F == 1 no kernel runs and
- *         `view_out` points at the context's inbox, read-only and valid until
- *         the next afd_source_dispatch on this context ("13. Single-FFN
- *         collect view" of the design page). With F > 1 the ordinary result
- *         is written to `out` and view_out->is_view = 0.
+ *   view  1 asks for the single-worker view: with F == 1 the combine writes
+ *         the context's inbox instead of `out`, and `view_out` points at it,
+ *         read-only and valid until the next afd_source_dispatch on this
+ *         context ("13. Single-FFN collect view" of the design page). With
+ *         F > 1 the ordinary result is written to `out` and
+ *         view_out->is_view = 0.
  *   view_out  host; filled on success (may be NULL when view = 0)
  * Errors: AFD_ERR_STATE (replies missing, or source already collected),
  * AFD_ERR_ARG, AFD_ERR_CUDA. */
@@ -258,8 +258,8 @@ AFD_API afd_status afd_source_collect(afd_ctx* ctx, int32_t source, void* out, i
 
 /* Every source's result at once: for each source s the same as
  * afd_source_collect(s, outs[s], view, ...), with one combine launch for all
- * sources when F > 1 (on one GPU the sources' combines are independent, so
- * they can share a launch). Every source must still be uncollected.
+ * sources (on one GPU the sources' combines are independent, so they can
+ * share a launch). Every source must still be uncollected.
  *   outs   host array of A device pointers, BF16 [T_s, H] each; an entry may
  *          be NULL for a source with T = 0, or when view = 1 and F == 1
  *   view   as in afd_source_collect
