@@ -219,6 +219,9 @@ AFD_API afd_status afd_worker_receive(afd_ctx* ctx, int32_t worker, int32_t buck
  *   rows      device BF16 [num_rows, H], unweighted expert outputs; row r
  *             answers received row r. Padding rows are never read. It may be
  *             the received rows themselves (an identity expert, BF16 only).
+ *             The library reads it until the combine of the exchange's last
+ *             collected source has completed; it must stay unchanged until
+ *             then.
  *   num_rows  must equal the afd_recv.num_rows of this worker's receive
  *   receipt   must equal the afd_recv.receipt of this worker's receive
  * The library applies each routing weight exactly once, in the combine,
@@ -251,6 +254,12 @@ typedef struct afd_view {
  *         F > 1 the ordinary result is written to `out` and
  *         view_out->is_view = 0.
  *   view_out  host; filled on success (may be NULL when view = 0)
+ * When the previous call on this context was a collect of the same exchange
+ * that launched a combine on the same stream, this call's combine starts
+ * without waiting for that one (both only read the replies) and completes
+ * after it, so stream order still holds for whatever follows. Work enqueued on
+ * the stream between the two calls must therefore not write the reply rows
+ * or this source's `out`.
  * Errors: AFD_ERR_STATE (replies missing, or source already collected),
  * AFD_ERR_ARG, AFD_ERR_CUDA. */
 AFD_API afd_status afd_source_collect(afd_ctx* ctx, int32_t source, void* out, int32_t view,
