@@ -211,7 +211,7 @@ __device__ __forceinline__ void e4m3_round_trip2(float& a, float& b) {
 // row pointers, weights and workers (-1 for a skipped route). Returns the
 // valid routes as bits.
 __device__ __forceinline__ uint32_t token_routes(const CombineParams& p, int2 r, const uint16_t* (&rowp)[kGroup],
-                                                 float (&wk)[kGroup], int (&wf)[kGroup]) {
+                                                 float (&wk)[kGroup]) {
   uint32_t okmask = 0u;
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) {
@@ -219,9 +219,50 @@ __device__ __forceinline__ uint32_t token_routes(const CombineParams& p, int2 r,
     wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, j));
     const bool ok = (j < p.K) && (c >= 0);
     okmask |= (ok ? 1u : 0u) << j;
-    wf[j] = ok ? (c >> kWorkerShift) : -1;
     rowp[j] = ok ? p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
   }
+  return okmask;
+}
+
+// The two-stage modes take a token's routes in summation order instead:
+// grouped by worker, the groups in the order of each worker's last route,
+// ascending k inside a group (the order of the design page's section 19).
+// Slot j gets route perm[j]; bit j of *bnd marks the last slot of a group.
+// Lane k < K ranks its own route by key (last route of its worker) * 8 + k
+// (skipped routes after all others), and a ballot per slot finds the lane
+// that holds it.
+__device__ __forceinline__ uint32_t token_routes_grouped(const CombineParams& p, int2 r,
+                                                         const uint16_t* (&rowp)[kGroup], float (&wk)[kGroup],
+                                                         uint32_t& bnd) {
+  const int lane = threadIdx.x & 31;
+  const int wf_me = (lane < p.K && r.x >= 0) ? (r.x >> kWorkerShift) : -1;
+  int wf[kGroup];
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) wf[j] = __shfl_sync(0xffffffffu, wf_me, j);
+  int last = lane;
+#pragma unroll
+  for (int j = 1; j < kGroup; ++j) last = (j > lane && wf[j] == wf_me) ? j : last;
+  const int key_me = wf_me >= 0 ? last * kGroup + lane : kGroup * kGroup + lane;
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) rank += __shfl_sync(0xffffffffu, key_me, j) < key_me ? 1 : 0;
+  uint32_t okmask = 0u;
+  int prev_wf = -1;
+  bnd = 0u;
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) {
+    const int src = __ffs(__ballot_sync(0xffffffffu, lane < kGroup && rank == j)) - 1;
+    const int c = __shfl_sync(0xffffffffu, r.x, src);
+    wk[j] = __int_as_float(__shfl_sync(0xffffffffu, r.y, src));
+    const bool ok = (src < p.K) && (c >= 0);
+    const int w = ok ? (c >> kWorkerShift) : -1;
+    okmask |= (ok ? 1u : 0u) << j;
+    rowp[j] = ok ? p.reply[w] + (int64_t)(c & kRowMask) * p.H : p.reply[0];
+    // the slot before ends its group when this one belongs to another worker
+    if (j > 0 && prev_wf >= 0 && w != prev_wf) bnd |= 1u << (j - 1);
+    prev_wf = w;
+  }
+  if (prev_wf >= 0) bnd |= 1u << (kGroup - 1);
   return okmask;
 }
 
@@ -241,7 +282,7 @@ __device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* c
 // then rounded to BF16 once.
 template <int kMode>
 __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGroup], const float (&wk)[kGroup],
-                                        const int (&wf)[kGroup], uint32_t okmask, int v) {
+                                        uint32_t bnd, uint32_t okmask, int v) {
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -250,19 +291,15 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
     for (int j = 0; j < kGroup; ++j)
       if ((okmask >> j) & 1u) fma8(acc, wk[j], buf[j]);
   } else {
+    // slots in summation order (token_routes_grouped): one worker's partial
+    // is an FP32 chain over its run of slots, finished at the run's end
+    float part[8];
 #pragma unroll
-    for (int k = 0; k < kGroup; ++k) {
-      if (wf[k] < 0) continue;
-      bool last = true;
+    for (int e = 0; e < 8; ++e) part[e] = 0.0f;
 #pragma unroll
-      for (int j = k + 1; j < kGroup; ++j) last = last && (wf[j] != wf[k]);
-      if (!last) continue;
-      float part[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) part[e] = 0.0f;
-#pragma unroll
-      for (int j = 0; j <= k; ++j)
-        if (wf[j] == wf[k]) fma8(part, wk[j], buf[j]);
+    for (int j = 0; j < kGroup; ++j) {
+      if ((okmask >> j) & 1u) fma8(part, wk[j], buf[j]);
+      if (!((bnd >> j) & 1u)) continue;  // the same for the whole warp
 #pragma unroll
       for (int e = 0; e < 8; ++e) part[e] = bf16_round(part[e]);
       if (kMode == AFD_COMBINE_TWO_STAGE_FP8) {
@@ -283,7 +320,10 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
         }
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = acc[e] + part[e];
+      for (int e = 0; e < 8; ++e) {
+        acc[e] = acc[e] + part[e];
+        part[e] = 0.0f;
+      }
     }
   }
   uint4 o;
@@ -316,8 +356,9 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_S
     if (lane < K) r = __ldcg(p.routes[s] + (int64_t)t * K + lane);
     const uint16_t* rowp[kGroup];
     float wk[kGroup];
-    int wf[kGroup];
-    const uint32_t okmask = token_routes(p, r, rowp, wk, wf);
+    uint32_t bnd = 0u;
+    const uint32_t okmask = kMode == AFD_COMBINE_FUSED ? token_routes(p, r, rowp, wk)
+                                                       : token_routes_grouped(p, r, rowp, wk, bnd);
     uint4* out_row = reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]) + seg0 * 32;
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
@@ -326,11 +367,11 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_S
     int seg = 0;
     for (; seg + 2 <= nseg; seg += 2) {
       load_seg(b, rowp, okmask, (seg + 1) * 32 + lane, p.early);
-      sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
+      sum_seg<kMode>(out_row, a, wk, bnd, okmask, seg * 32 + lane);
       if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane, p.early);
-      sum_seg<kMode>(out_row, b, wk, wf, okmask, (seg + 1) * 32 + lane);
+      sum_seg<kMode>(out_row, b, wk, bnd, okmask, (seg + 1) * 32 + lane);
     }
-    if (seg < nseg) sum_seg<kMode>(out_row, a, wk, wf, okmask, seg * 32 + lane);
+    if (seg < nseg) sum_seg<kMode>(out_row, a, wk, bnd, okmask, seg * 32 + lane);
   }
   combine_end(p);
 }
@@ -356,11 +397,12 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
     if (lane < K) r = __ldcg(p.routes[s] + (int64_t)t * K + lane);
     const uint16_t* rowp[kGroup];
     float wk[kGroup];
-    int wf[kGroup];
-    const uint32_t okmask = token_routes(p, r, rowp, wk, wf);
+    uint32_t bnd = 0u;
+    const uint32_t okmask = kMode == AFD_COMBINE_FUSED ? token_routes(p, r, rowp, wk)
+                                                       : token_routes_grouped(p, r, rowp, wk, bnd);
     uint4 buf[kGroup];
     load_seg(buf, rowp, okmask, seg * 32 + lane, p.early);
-    sum_seg<kMode>(reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]), buf, wk, wf,
+    sum_seg<kMode>(reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]), buf, wk, bnd,
                    okmask, seg * 32 + lane);
   }
   combine_end(p);
