@@ -335,7 +335,10 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
 }
 
 template <int kMode>
-__global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED ? 0 : AFD_TWO_STAGE_BLOCKS) combine_token_kernel(const __grid_constant__ CombineParams p) {
+__global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED               ? 0
+                                     : kMode == AFD_COMBINE_TWO_STAGE_FP8 ? AFD_TWO_STAGE_FP8_BLOCKS
+                                                                          : AFD_TWO_STAGE_BLOCKS)
+    combine_token_kernel(const __grid_constant__ CombineParams p) {
   combine_begin(p);
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;

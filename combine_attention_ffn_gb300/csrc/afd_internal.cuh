@@ -39,6 +39,9 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_TWO_STAGE_BLOCKS
 #define AFD_TWO_STAGE_BLOCKS 7    // resident two-warp blocks per SM asked of the two-stage per-token combine
 #endif
+#ifndef AFD_TWO_STAGE_FP8_BLOCKS
+#define AFD_TWO_STAGE_FP8_BLOCKS 8  // the same, with E4M3 partials
+#endif
 #ifndef AFD_EARLY_LOADS
 #define AFD_EARLY_LOADS 0         // 1: an early-started combine reads replies with ld.global.cg (L2 only)
 #endif
