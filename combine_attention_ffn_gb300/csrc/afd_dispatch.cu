@@ -502,11 +502,14 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
   } else {
     pdl_launch_dependents();
   }
-  // the source rows are inputs, not layout outputs: load the first one while
-  // the layout is still running
-  if (lane == 0 && gwarp < p.total_tokens) {
+  // the source rows (and FP8 scales) are inputs, not layout outputs: load
+  // the first token's while the layout is still running
+  float sc_first = 0.0f;
+  if (gwarp < p.total_tokens) {
     const int s0 = source_of_token(p, gwarp);
-    bulk_load(buf, p.src[s0].x + (int64_t)(gwarp - p.src[s0].tok_off) * rb, rb, mbar);
+    const int t0 = gwarp - p.src[s0].tok_off;
+    if (lane == 0) bulk_load(buf, p.src[s0].x + (int64_t)t0 * rb, rb, mbar);
+    if (lane < p.nscale) sc_first = p.src[s0].scale[(int64_t)t0 * p.src[s0].sst + (int64_t)lane * p.src[s0].ssb];
   }
   if (!kCached) pdl_wait();  // the layout kernel's route codes
 
@@ -540,30 +543,37 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
           p.routes[(int64_t)gt * K + lane] = make_int2(-1, 0);
       }
     }
-    for (int b0 = 0; b0 < p.nscale; b0 += 32) {  // FP8: the row's block scales follow it
+    if (copying) {
+      if (!wait_phase_warp(mbar, parity, p.wait_polls)) {
+        // the row's load did not complete in time: report it, and wait
+        // (bounded by time) for the load still in flight before the buffer
+        // is abandoned
+        if (lane == 0) atomicMin(p.err, route_error_key(s, t, 0, kErrTimeout));
+        drain_phase_warp(mbar, parity);
+        copying = false;
+      } else {
+        parity ^= 1u;
+        if (code >= 0)
+          bulk_store(p.rows + ((int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)) * rb, buf, rb);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    }
+    // FP8: the row's block scales follow it, written while its bulk stores run
+    for (int b0 = 0; b0 < p.nscale; b0 += 32) {
       const int b = b0 + lane;
-      const float sc = b < p.nscale ? src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb] : 0.0f;
+      float sc = 0.0f;
+      if (b < p.nscale)
+        sc = (gt == gwarp && b0 == 0) ? sc_first : src.scale[(int64_t)t * src.sst + (int64_t)b * src.ssb];
       for (int k = 0; k < K; ++k) {
         const int c = __shfl_sync(0xffffffffu, code, k);
         if (c >= 0 && b < p.nscale)
           p.row_scales[((int64_t)(c >> kWorkerShift) * p.R_arena + (c & kRowMask)) * p.nscale + b] = sc;
       }
     }
-    if (!copying) continue;
-    if (!wait_phase_warp(mbar, parity, p.wait_polls)) {
-      // the row's load did not complete in time: report it, and wait (bounded
-      // by time) for the load still in flight before the buffer is abandoned
-      if (lane == 0) atomicMin(p.err, route_error_key(s, t, 0, kErrTimeout));
-      drain_phase_warp(mbar, parity);
-      copying = false;
-      continue;
+    if (copying) {
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // this lane's copies have read buf
+      __syncwarp();
     }
-    parity ^= 1u;
-    if (code >= 0)
-      bulk_store(p.rows + ((int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)) * rb, buf, rb);
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // this lane's copies have read buf
-    __syncwarp();
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this lane's copies are complete
   if (!kCached) fill_padding(p, p.ends);
