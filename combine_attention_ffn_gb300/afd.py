@@ -37,7 +37,7 @@ EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispa
            "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
            "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc",
-           "afd_set_wait_limit")
+           "afd_set_wait_limit", "afd_phase_stamps")
 
 
 class AfdError(RuntimeError):
@@ -98,6 +98,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_version": (i32, []),
         "afd_route_layout_noalloc": (i32, [v, i32, i32, i32, i32, i32, v, v, v, v]),
         "afd_set_wait_limit": (i32, [v, i32]),
+        "afd_phase_stamps": (i32, [v, P(u64), i64, i32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -105,6 +106,19 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     if path is None:
         _lib = lib
     return lib
+
+
+def use_library(path: str) -> ctypes.CDLL:
+    """Makes the library at `path` (e.g. the phase-timer build) the one every
+    Buffer created afterwards calls."""
+    global _lib
+    _lib = load_library(path)
+    return _lib
+
+
+# afd_phase_stamps: [kind][block][point] (afd.h)
+STAMP_KINDS = ("dispatch", "scatter", "combine", "combine-early")
+STAMP_SHAPE = (4, 4096, 8)
 
 
 class _Context:
@@ -359,6 +373,16 @@ class Buffer:
 
     def reset_exchange(self) -> None:
         self._check(self._lib.afd_reset_exchange(self._h), "reset_exchange")
+
+    def phase_stamps(self, clear: bool = False) -> np.ndarray:
+        """The phase-timer build's %globaltimer stamps, uint64 STAMP_SHAPE
+        (afd_phase_stamps); synchronizes the device. Raises AfdError with
+        ERR_UNSUPPORTED on the default build."""
+        out = np.zeros(STAMP_SHAPE, dtype=np.uint64)
+        st = self._lib.afd_phase_stamps(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                        out.size, int(bool(clear)))
+        self._check(st, "phase_stamps")
+        return out
 
     def set_wait_limit(self, polls: int) -> None:
         """Polls of each bulk row load before the scatter reports AFD_ERR_TIMEOUT

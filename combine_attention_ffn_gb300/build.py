@@ -18,6 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libafd.so")
+# The diagnostic phase-timer build (-DAFD_PHASE_TIMERS=1), kept apart.
+BUILD_TIMERS = os.path.join(HERE, "_build", "timers")
+LIB_TIMERS = os.path.join(HERE, "libafd_timers.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -40,8 +43,8 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def _compile(src: str, extra: list[str]) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], build_dir: str = BUILD) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -50,18 +53,18 @@ def _compile(src: str, extra: list[str]) -> tuple[str, str]:
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
-          out: str = LIB) -> str:
+          out: str = LIB, build_dir: str = BUILD) -> str:
     """Compiles every csrc/*.cu and links libafd.so. Returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     if not force and os.path.exists(out):
         newest = max(os.path.getmtime(p) for p in _deps())
         if os.path.getmtime(out) >= newest:
             return out
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra or []), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra or [], build_dir), srcs))
     log = "\n".join(r[1] for r in results)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as fh:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as fh:
         fh.write(log)
     if verbose:
         print(log)
@@ -72,6 +75,12 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, out)
     return out
+
+
+def build_timers(force: bool = False) -> str:
+    """The diagnostic library with phase timers (libafd_timers.so): the same
+    kernels plus %globaltimer stamps (see afd_phase_stamps in afd.h)."""
+    return build(force=force, extra=["-DAFD_PHASE_TIMERS=1"], out=LIB_TIMERS, build_dir=BUILD_TIMERS)
 
 
 if __name__ == "__main__":

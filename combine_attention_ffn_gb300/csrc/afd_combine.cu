@@ -33,6 +33,22 @@
 #include "afd_internal.cuh"
 
 namespace afd {
+
+#if AFD_PHASE_TIMERS
+// [0: a combine that waits first, 1: an early-started combine][block][point]
+__device__ unsigned long long g_combine_stamps[2][kStampBlocks][kStampPoints];
+
+cudaError_t read_combine_stamps(unsigned long long* host, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_combine_stamps, sizeof(g_combine_stamps));
+  if (e == cudaSuccess && clear) {
+    void* d = nullptr;
+    e = cudaGetSymbolAddress(&d, g_combine_stamps);
+    if (e == cudaSuccess) e = cudaMemset(d, 0, sizeof(g_combine_stamps));
+  }
+  return e;
+}
+#endif
+
 namespace {
 
 constexpr int kGroup = 8;  // routes whose loads are issued together
@@ -69,6 +85,7 @@ __device__ __forceinline__ uint4 ld_reply(const uint4* p, bool early) {
 }
 
 __device__ __forceinline__ void combine_begin(const CombineParams& p) {
+  AFD_STAMP(g_combine_stamps, p.early ? 1 : 0, 0);
   if (!p.early) {
     pdl_wait();
   } else {
@@ -79,9 +96,12 @@ __device__ __forceinline__ void combine_begin(const CombineParams& p) {
 #endif
   }
   pdl_launch_dependents();
+  AFD_STAMP(g_combine_stamps, p.early ? 1 : 0, 1);
 }
 __device__ __forceinline__ void combine_end(const CombineParams& p) {
+  AFD_STAMP(g_combine_stamps, p.early ? 1 : 0, 2);  // this block's sums are stored
   if (p.early) pdl_wait();
+  AFD_STAMP(g_combine_stamps, p.early ? 1 : 0, 3);
 }
 
 __device__ __forceinline__ int source_of(const CombineParams& p, int gt) {

@@ -36,6 +36,22 @@
 #include "afd_internal.cuh"
 
 namespace afd {
+
+#if AFD_PHASE_TIMERS
+// [kind 0: first dispatch kernel, kind 1: scatter][block][point]
+__device__ unsigned long long g_dispatch_stamps[2][kStampBlocks][kStampPoints];
+
+cudaError_t read_dispatch_stamps(unsigned long long* host, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_dispatch_stamps, sizeof(g_dispatch_stamps));
+  if (e == cudaSuccess && clear) {
+    void* d = nullptr;
+    e = cudaGetSymbolAddress(&d, g_dispatch_stamps);
+    if (e == cudaSuccess) e = cudaMemset(d, 0, sizeof(g_dispatch_stamps));
+  }
+  return e;
+}
+#endif
+
 namespace {
 
 __device__ __forceinline__ int source_of_token(const DispatchParams& p, int gt) {
@@ -275,6 +291,8 @@ __device__ __forceinline__ int layout_tpc(const DispatchParams& p) {
 }
 
 __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_constant__ DispatchParams p) {
+  AFD_STAMP_REGS;
+  AFD_STAMP_REG(0);
   extern __shared__ __align__(16) uint32_t smem[];
   const int E = p.E, K = p.K, N = p.total_tokens;
   uint32_t* mask = smem;                                        // [8][E]
@@ -289,6 +307,7 @@ __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_
   // the IDs, weights and rows, or still read the arenas) before touching
   // memory, and only then lets the scatter launch.
   pdl_wait();
+  AFD_STAMP_REG(1);
   pdl_launch_dependents();
 
   const int n = gridDim.x;
@@ -318,6 +337,7 @@ __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_
     int e8[8];
     const uint32_t valid = live ? mark_token(ids, K, E, mask + warp * E, lane, s, t, p.err, e8) : 0u;
     __syncthreads();
+    if (c0 == lo) AFD_STAMP_REG(2);  // the first slice's IDs read and marked
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       int run = cnt[e];
 #pragma unroll
@@ -352,9 +372,11 @@ __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_
     __syncthreads();  // the masks are cleared for the next slice
   }
 
+  AFD_STAMP_REG(3);
   // Every CTA's counts are final: read them all through the cluster.
   cluster_arrive();
   cluster_wait();
+  AFD_STAMP_REG(4);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int v[kLayoutMaxCtas];
 #pragma unroll
@@ -368,11 +390,13 @@ __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_
     before[e] = b;
     total[e] = all;
   }
+  AFD_STAMP_REG(5);
   // no CTA may leave (and free its shared memory) while others still read it
   cluster_arrive();
   __syncthreads();
   worker_scan(p, total, start, r == 0);
   __syncthreads();
+  AFD_STAMP_REG(6);
   // this CTA's first code per expert: (worker << 24) | its first row
   for (int e = threadIdx.x; e < E; e += blockDim.x) start[e] = ((e / p.Ef) << kWorkerShift) + start[e] + before[e];
   __syncthreads();
@@ -382,10 +406,13 @@ __global__ void __launch_bounds__(kChunk, 1) cluster_layout_kernel(const __grid_
     p.route_tmp[(int64_t)lo * K + i] =
         c < 0 ? -1 : start[c >> kLocalRankBits] + (c & ((1 << kLocalRankBits) - 1));
   }
+  AFD_STAMP_REG(7);
   cluster_wait();
+  AFD_STAMP_REGS_STORE(g_dispatch_stamps, 0);
 }
 
 __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid_constant__ DispatchParams p) {
+  AFD_STAMP(g_dispatch_stamps, 1, 0);
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -398,6 +425,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   float pre_w = 0.0f;
   const bool have_pre = preload_first(p, gwarp, pre, pre_w);
   pdl_wait();  // the layout kernel's outputs
+  AFD_STAMP(g_dispatch_stamps, 1, 1);
 
   auto code_of = [&](int gt) { return lane < K ? __ldcg(p.route_tmp + (int64_t)gt * K + lane) : -1; };
   int gt = gwarp;
@@ -407,6 +435,7 @@ __global__ void __launch_bounds__(AFD_SCATTER_BLOCK) scatter_kernel(const __grid
   }
   for (; gt < p.total_tokens; gt += nwarps) scatter_token<false>(p, gt, code_of(gt), 0.0f, pre);
   fill_padding(p, p.ends);
+  AFD_STAMP(g_dispatch_stamps, 1, 5);
 }
 
 // ---- bulk-copy scatter (rows of at most kBulkRowMax bytes in device memory)
@@ -453,16 +482,11 @@ __device__ __forceinline__ bool wait_phase_warp(uint64_t* mbar, uint32_t parity,
 // (kDrainNs of the global timer), so that it ends however long each poll
 // suspends the thread. The warp decides together, as above.
 constexpr unsigned long long kDrainNs = 2000000000ull;  // 2 s
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 __device__ __forceinline__ bool drain_phase_warp(uint64_t* mbar, uint32_t parity) {
-  const unsigned long long t0 = global_ns();
+  const unsigned long long t0 = global_timer_ns();
   for (;;) {
     if (__all_sync(0xffffffffu, phase_done(mbar, parity))) return true;
-    const unsigned long long dt = global_ns() - t0;  // lane 0's clock decides for the warp
+    const unsigned long long dt = global_timer_ns() - t0;  // lane 0's clock decides for the warp
     if (__shfl_sync(0xffffffffu, dt, 0) > kDrainNs) return false;
   }
 }
@@ -483,6 +507,7 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
 // replace the old ones in both receipts.
 template <bool kCached>
 __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant__ DispatchParams p) {
+  if (!kCached) AFD_STAMP(g_dispatch_stamps, 1, 0);
   extern __shared__ __align__(128) uint8_t bsm[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(bsm) + wib;       // one barrier per warp
@@ -512,6 +537,7 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
     if (lane < p.nscale) sc_first = p.src[s0].scale[(int64_t)t0 * p.src[s0].sst + (int64_t)lane * p.src[s0].ssb];
   }
   if (!kCached) pdl_wait();  // the layout kernel's route codes
+  if (!kCached) AFD_STAMP(g_dispatch_stamps, 1, 1);
 
   uint32_t parity = 0;
   // false once a wait of this warp gave up: the warp then writes only the
@@ -552,6 +578,7 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
         drain_phase_warp(mbar, parity);
         copying = false;
       } else {
+        if (!kCached && gt == gwarp) AFD_STAMP(g_dispatch_stamps, 1, 2);  // first row in shared memory
         parity ^= 1u;
         if (code >= 0)
           bulk_store(p.rows + ((int64_t)(code >> kWorkerShift) * p.R_arena + (code & kRowMask)) * rb, buf, rb);
@@ -575,8 +602,11 @@ __global__ void __launch_bounds__(64) scatter_bulk_kernel(const __grid_constant_
       __syncwarp();
     }
   }
+  if (!kCached) AFD_STAMP(g_dispatch_stamps, 1, 3);
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // this lane's copies are complete
+  if (!kCached) AFD_STAMP(g_dispatch_stamps, 1, 4);
   if (!kCached) fill_padding(p, p.ends);
+  if (!kCached) AFD_STAMP(g_dispatch_stamps, 1, 5);
 }
 
 // Copies token (s, t)'s row to one route's row (code = (worker << 24) | row,
@@ -621,7 +651,9 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   uint16_t* wbase = reinterpret_cast<uint16_t*>(sh_total + E);    // [8][E]
   uint16_t* ccnt = wbase + kChunkWarps * E;                // [G][E]
 
+  AFD_STAMP(g_dispatch_stamps, 0, 0);
   pdl_wait();  // the work before the exchange (see cluster_layout_kernel)
+  AFD_STAMP(g_dispatch_stamps, 0, 1);
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long* err = blockIdx.x == 0 ? p.err : nullptr;
@@ -748,6 +780,7 @@ __global__ void __launch_bounds__(256) dispatch_small_kernel(const __grid_consta
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_total[e] += sh_start[e];  // ends
   __syncthreads();
   fill_padding(p, sh_total);
+  AFD_STAMP(g_dispatch_stamps, 0, 7);
 }
 
 // ---------------------------------------------------------------- cached path
@@ -845,7 +878,9 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
   uint32_t* mask = tsm;                                     // [E]
   int32_t* sh_start = reinterpret_cast<int32_t*>(mask + E);  // [E]
   int32_t* sh_end = sh_start + E;                           // [E]
+  AFD_STAMP(g_dispatch_stamps, 0, 0);
   pdl_wait();  // the work before the exchange (see cluster_layout_kernel)
+  AFD_STAMP(g_dispatch_stamps, 0, 1);
   pdl_launch_dependents();
   const int lane = threadIdx.x;
 
@@ -925,6 +960,7 @@ __global__ void __launch_bounds__(32) dispatch_tiny_kernel(const __grid_constant
       }
     }
   }
+  AFD_STAMP(g_dispatch_stamps, 0, 7);
 }
 
 size_t layout_smem(int E) { return (size_t)kChunkWarps * E * 8 + (size_t)4 * E * 4 + (size_t)kLayoutCodesMax * 4; }

@@ -140,6 +140,18 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t configure_dispatch_kernels(int* max_ctas);
+#ifndef AFD_PHASE_TIMERS
+#define AFD_PHASE_TIMERS 0  // 1: the diagnostic build with %globaltimer stamps (afd_device.cuh)
+#endif
+constexpr int kStampKinds = 4;     // first dispatch kernel, scatter, waiting combine, early combine
+constexpr int kStampBlocks = 4096;  // blocks recorded per kind
+constexpr int kStampPoints = 8;     // points recorded per block
+#if AFD_PHASE_TIMERS
+// Phase-timer builds: copy out (and optionally zero) each translation unit's
+// stamps, [2][kStampBlocks][kStampPoints] each.
+cudaError_t read_dispatch_stamps(unsigned long long* host, bool clear);
+cudaError_t read_combine_stamps(unsigned long long* host, bool clear);
+#endif
 cudaError_t configure_combine_kernels();
 
 }  // namespace afd

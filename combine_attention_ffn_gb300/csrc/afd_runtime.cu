@@ -816,6 +816,28 @@ afd_status afd_set_wait_limit(afd_ctx* c, int32_t polls) {
   return AFD_OK;
 }
 
+afd_status afd_phase_stamps(afd_ctx* c, uint64_t* host, int64_t count, int32_t clear) {
+#if AFD_PHASE_TIMERS
+  if (!c || !host) return AFD_ERR_ARG;
+  const int64_t half = 2ll * afd::kStampBlocks * afd::kStampPoints;
+  if (count < 2 * half) return fail(c, AFD_ERR_ARG, "count must be at least %lld", (long long)(2 * half));
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return fail(c, AFD_ERR_CUDA, "cannot select device %d", c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = afd::read_dispatch_stamps(reinterpret_cast<unsigned long long*>(host), clear != 0);
+  if (e == cudaSuccess) e = afd::read_combine_stamps(reinterpret_cast<unsigned long long*>(host + half), clear != 0);
+  if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(c, e, "reading the phase stamps");
+  return AFD_OK;
+#else
+  (void)c;
+  (void)host;
+  (void)count;
+  (void)clear;
+  return AFD_ERR_UNSUPPORTED;
+#endif
+}
+
 afd_status afd_clear_error(afd_ctx* c, afd_stream stream_) {
   if (!c) return AFD_ERR_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

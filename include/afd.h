@@ -301,6 +301,24 @@ AFD_API afd_status afd_get_error(afd_ctx* ctx, int32_t* code, int32_t* source, i
  * Errors: AFD_ERR_ARG (polls < 0). */
 AFD_API afd_status afd_set_wait_limit(afd_ctx* ctx, int32_t polls);
 
+/* Diagnostic: the phase stamps of a library built with -DAFD_PHASE_TIMERS=1
+ * (%globaltimer, ns). Synchronizes the device, then copies the stamps to
+ * `host` as uint64 [4][4096][8]: [kind][block][point], 0 where nothing was
+ * recorded; clear = 1 also zeroes them. Kinds: 0 the exchange's first
+ * dispatch kernel (points 0 start, 1 dependency wait passed, 2 first IDs
+ * marked, 3 counted, 4 cluster barrier passed, 5 counts of all CTAs read,
+ * 6 scan done, 7 route codes written; the one-kernel dispatches record 0, 1
+ * and 7), 1 the scatter (0 start, 1 wait passed, 2 first row in shared
+ * memory, 3 all stores issued, 4 stores complete, 5 end), 2 a combine that
+ * waits first and 3 an early-started combine (0 start, 1 wait passed or
+ * fence done, 2 sums stored, 3 end). The stamps are global to the process;
+ * the last launch of a kind overwrites the earlier ones; blocks past 4096
+ * are not recorded.
+ *   host   host uint64 array of `count` >= 131072 elements
+ * Errors: AFD_ERR_UNSUPPORTED when built without phase timers (whatever the
+ * arguments), AFD_ERR_ARG, AFD_ERR_CUDA. */
+AFD_API afd_status afd_phase_stamps(afd_ctx* ctx, uint64_t* host, int64_t count, int32_t clear);
+
 /* Clears the sticky route error (enqueued on `stream`). */
 AFD_API afd_status afd_clear_error(afd_ctx* ctx, afd_stream stream);
 

@@ -110,3 +110,18 @@ def test_noalloc_size_limits_are_host_checks(lib_path):
                               (4, 2, 8, 2, 0)):
         st = lib.afd_route_layout_noalloc(bogus, T, K, E, F, alpha, bogus, bogus, bogus, None)
         assert st == afd.ERR_ARG, (T, K, E, F, alpha)
+
+
+def test_phase_stamps_only_in_the_timer_build(lib_path):
+    """The default build has no phase timers: afd_phase_stamps answers
+    AFD_ERR_UNSUPPORTED without touching a device. The timer build compiles
+    (for sm_103a, here without a GPU) and exports the same entry points."""
+    from combine_attention_ffn_gb300 import afd, build
+
+    lib = afd.load_library(lib_path)
+    assert lib.afd_phase_stamps(None, None, 0, 0) == afd.ERR_UNSUPPORTED
+    timers = build.build_timers()
+    assert timers != lib_path and os.path.exists(timers)
+    out = subprocess.run(["nm", "-D", "--defined-only", timers], capture_output=True, text=True,
+                         check=True).stdout
+    assert set(declared_functions()) <= set(re.findall(r"\bT (afd_\w+)$", out, flags=re.M))
