@@ -62,7 +62,7 @@ static_assert(kChunk <= (1 << kRankBits), "rank in chunk must fit its field");
 // Every kernel of the library asks for the same split of each SM's unified
 // L1 / shared memory. The kernels of one exchange overlap on the same SMs
 // through programmatic dependent launch; when their preferred splits differ
-// (the layout needs tens of KB of shared memory, the copy kernels none), an
+// (the layout needs tens of KB of shared memory, the combines none), an
 // SM cannot take blocks of the next kernel until it has drained and changed
 // its split, which cost up to 6 us per round trip.
 constexpr int kSharedCarveout = 50;  // percent of the maximum shared memory

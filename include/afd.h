@@ -40,9 +40,10 @@
  *   - Host-detected errors return at once and enqueue nothing.
  *   - The caller owns every pointer it passes; each must stay valid and
  *     unchanged until the GPU work that reads or writes it has completed.
- *   - The context owns the receive arenas, the receipts, the combine inboxes
- *     and the pinned host counts; pointers it returns stay valid until
- *     afd_destroy, and their contents until the exchange's rules below say.
+ *   - The context owns the receive arenas, the receipts, the single-worker
+ *     view inboxes and the pinned host counts; pointers it returns stay
+ *     valid until afd_destroy, and their contents until the exchange's rules
+ *     below say.
  *   - All calls are host-thread-unsafe on one context: serialize them.
  */
 #ifndef AFD_H
