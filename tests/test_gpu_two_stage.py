@@ -92,3 +92,24 @@ def test_two_stage_rejects_large_top_k():
     with pytest.raises(afd.AfdError) as ei:
         afd.Buffer(2, 2, 64, 9, 256, 16, 1, "bf16", combine_mode=afd.COMBINE_TWO_STAGE)
     assert ei.value.status == afd.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("F,T", [(8, 300), (16, 1024), (64, 700)])
+def test_two_stage_many_workers(mode, F, T):
+    """Many workers: a token's eight routes fall on up to eight workers, in
+    any interleaving, so the per-token regrouping into summation order has up
+    to eight runs; 300 tokens per source take the segmented kernel, 1,024 and
+    700 the per-token one."""
+    wl = W.Workload(f"2A{F}F", A=2, F=F, E=128, K=8, H=512, alpha=4, capacity=T, bucket=T,
+                    T=(T, T // 2 + 1), routing="uniform" if F == 8 else "zipf", drop=0.1, seed=900 + F)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE, combine_mode=mode)
+    buf = GH.make_buffer(wl, combine_mode=mode)
+    try:
+        recvs, _, results = GH.run_exchange(buf, wl, GH.to_device(inp), mode=GH.SCALE)
+        torch.cuda.synchronize()
+        GH.check_layout(wl, GH.snapshot(recvs), exp, False, buf)
+        GH.check_outputs(wl, results, exp)
+    finally:
+        buf.close()
