@@ -164,19 +164,25 @@ def kernel_traffic(kernel: str, workload: str):
 
 class L2Flush:
     """Evicts L2 (129 MB) between timed steps, outside the steps' events: a
-    256 MB write, then a 256 MB read, so that the write's dirty lines are
-    written back before the step starts instead of during it. The step then
-    finds none of its inputs in L2."""
+    256 MB write, then a 256 MB read of another buffer, so that the write's
+    dirty lines are written back before the step starts instead of during it.
+    The step then finds none of its inputs in L2. Both passes use an L2
+    evict-last policy (afd_l2_flush): the scatter writes its rows with that
+    policy, and ordinary writes and reads would not evict them."""
 
     def __init__(self, torch, dev):
-        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        self.r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
-        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+        self.scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         self.torch = torch
+        from combine_attention_ffn_gb300 import afd
+
+        self.lib = afd.load_library(afd.LIB_PATH)  # the in-tree library, whichever one is in use
+        self.afd = afd
 
     def __call__(self):
-        self.w.zero_()
-        self.torch.sum(self.r, dim=0, out=self.acc)
+        stream = self.torch.cuda.current_stream(self.scratch.device).cuda_stream
+        st = self.lib.afd_l2_flush(self.scratch.data_ptr(), self.scratch.numel(), stream)
+        if st != 0:
+            raise RuntimeError(f"afd_l2_flush failed (status {st})")
 
 
 class ClockSampler:
@@ -320,8 +326,9 @@ def run_reference(args):
     return 0
 
 
-L2_NOTE = ("flushed before every timed step (256 MB write, then 256 MB read so the write-backs "
-           "finish first; outside the step's events)")
+L2_NOTE = ("flushed before every timed step (256 MB write, then 256 MB read of another buffer so "
+           "the write-backs finish first, both with an L2 evict-last policy so that lines of every "
+           "priority are evicted; outside the step's events)")
 
 
 def workload_config(wl, combine: str = "fused") -> dict:

@@ -37,7 +37,7 @@ EXPORTS = ("afd_create", "afd_destroy", "afd_source_dispatch", "afd_source_dispa
            "afd_clear_error",
            "afd_reset_exchange", "afd_status_string", "afd_error_detail", "afd_arena_rows",
            "afd_recv_rows_for_bucket", "afd_version", "afd_route_layout_noalloc",
-           "afd_set_wait_limit", "afd_phase_stamps")
+           "afd_set_wait_limit", "afd_phase_stamps", "afd_l2_flush")
 
 
 class AfdError(RuntimeError):
@@ -99,6 +99,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "afd_route_layout_noalloc": (i32, [v, i32, i32, i32, i32, i32, v, v, v, v]),
         "afd_set_wait_limit": (i32, [v, i32]),
         "afd_phase_stamps": (i32, [v, P(u64), i64, i32]),
+        "afd_l2_flush": (i32, [v, i64, v]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)

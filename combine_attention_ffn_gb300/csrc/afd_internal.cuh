@@ -140,6 +140,9 @@ cudaError_t launch_dispatch(const DispatchParams& p, int sm_cap, cudaStream_t st
 cudaError_t launch_cached_scatter(const DispatchParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream);
 cudaError_t configure_dispatch_kernels(int* max_ctas);
+// afd_l2_flush: writes vecs 16-byte vectors at `scratch`, then reads the next
+// vecs, both with an L2 evict-last policy.
+cudaError_t launch_l2_flush(uint4* scratch, int64_t vecs, cudaStream_t stream);
 #ifndef AFD_PHASE_TIMERS
 #define AFD_PHASE_TIMERS 0  // 1: the diagnostic build with %globaltimer stamps (afd_device.cuh)
 #endif

@@ -816,6 +816,14 @@ afd_status afd_set_wait_limit(afd_ctx* c, int32_t polls) {
   return AFD_OK;
 }
 
+afd_status afd_l2_flush(void* scratch, int64_t bytes, afd_stream stream_) {
+  if (!scratch || bytes <= 0 || bytes % 32 != 0 || reinterpret_cast<uintptr_t>(scratch) % 16 != 0)
+    return AFD_ERR_ARG;
+  cudaError_t e = afd::launch_l2_flush(static_cast<uint4*>(scratch), bytes / 32,
+                                       reinterpret_cast<cudaStream_t>(stream_));
+  return e == cudaSuccess ? AFD_OK : AFD_ERR_CUDA;
+}
+
 afd_status afd_phase_stamps(afd_ctx* c, uint64_t* host, int64_t count, int32_t clear) {
 #if AFD_PHASE_TIMERS
   if (!c || !host) return AFD_ERR_ARG;

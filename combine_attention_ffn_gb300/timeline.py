@@ -81,8 +81,7 @@ def run(config: str, tokens: int, replays: int, back_to_back: bool, combine_mode
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         _exchange(buf, wl, xs, ids, ws, scs, outs, replies)
-    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # afd_l2_flush scratch
     for _ in range(3):
         g.replay()
     samples: dict = {}
@@ -93,8 +92,10 @@ def run(config: str, tokens: int, replays: int, back_to_back: bool, combine_mode
             torch.cuda.synchronize()
             buf.phase_stamps(clear=True)
         else:
-            flush_w.fill_(1)
-            flush_r.sum()
+            st = afd.load_library().afd_l2_flush(flush.data_ptr(), flush.numel(),
+                                                 torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise afd.AfdError(st, "afd_l2_flush")
             torch.cuda.synchronize()
             buf.phase_stamps(clear=True)
         g.replay()

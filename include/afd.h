@@ -302,6 +302,18 @@ AFD_API afd_status afd_get_error(afd_ctx* ctx, int32_t* code, int32_t* source, i
  * Errors: AFD_ERR_ARG (polls < 0). */
 AFD_API afd_status afd_set_wait_limit(afd_ctx* ctx, int32_t polls);
 
+/* For benchmarks that start every step with a cold L2: writes the first half
+ * of `scratch` and then reads the second half, 16 bytes at a time, both with
+ * an L2 evict-last policy (the one the scatter's row stores use, which
+ * ordinary writes and reads cannot evict). Afterwards L2 holds only clean
+ * lines of the second half: every earlier line, whatever its priority, has
+ * been evicted and, if dirty, written back. Enqueued on `stream`.
+ *   scratch  device memory of `bytes` bytes, 16-byte aligned; its contents
+ *            are overwritten
+ *   bytes    a multiple of 32, at least twice the L2 size for a full flush
+ * Errors: AFD_ERR_ARG (alignment or size), AFD_ERR_CUDA. */
+AFD_API afd_status afd_l2_flush(void* scratch, int64_t bytes, afd_stream stream);
+
 /* Diagnostic: the phase stamps of a library built with -DAFD_PHASE_TIMERS=1
  * (%globaltimer, ns). Synchronizes the device, then copies the stamps to
  * `host` as uint64 [4][4096][8]: [kind][block][point], 0 where nothing was

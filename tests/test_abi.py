@@ -125,3 +125,15 @@ def test_phase_stamps_only_in_the_timer_build(lib_path):
     out = subprocess.run(["nm", "-D", "--defined-only", timers], capture_output=True, text=True,
                          check=True).stdout
     assert set(declared_functions()) <= set(re.findall(r"\bT (afd_\w+)$", out, flags=re.M))
+
+
+def test_l2_flush_checks_arguments_on_the_host(lib_path):
+    """afd_l2_flush refuses a null, unaligned or badly sized scratch before
+    it touches a device."""
+    from combine_attention_ffn_gb300 import afd
+
+    lib = afd.load_library(lib_path)
+    assert lib.afd_l2_flush(None, 1 << 20, None) == afd.ERR_ARG
+    assert lib.afd_l2_flush(ctypes.c_void_p(0x1000), 0, None) == afd.ERR_ARG
+    assert lib.afd_l2_flush(ctypes.c_void_p(0x1000), 48, None) == afd.ERR_ARG      # not a multiple of 32
+    assert lib.afd_l2_flush(ctypes.c_void_p(0x1008), 1 << 20, None) == afd.ERR_ARG  # not 16-byte aligned

@@ -216,3 +216,29 @@ def test_scatter_wait_that_gives_up_is_reported_and_recoverable(name, T):
         assert buf.get_error() == (0, -1, -1, -1)
     finally:
         buf.close()
+
+
+def test_l2_flush_runs_and_keeps_the_exchange_exact():
+    """The benchmark flush (evict-last writes and reads of a scratch buffer,
+    then a discard of the read half) runs between exchanges without touching
+    anything but its scratch: the exchange after it still matches the
+    oracle."""
+    from combine_attention_ffn_gb300 import afd
+
+    lib = afd.load_library()
+    scratch = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    wl = W.named("2A2F", T=300)
+    inp = W.make_inputs(wl)
+    exp = GH.expected(inp, GH.SCALE)
+    buf = GH.make_buffer(wl)
+    try:
+        dev = GH.to_device(inp)
+        outs = GH.alloc_outs(wl)
+        for _ in range(2):
+            st = lib.afd_l2_flush(scratch.data_ptr(), scratch.numel(), torch.cuda.current_stream().cuda_stream)
+            assert st == afd.OK
+            recvs, _, results = GH.run_exchange(buf, wl, dev, mode=GH.SCALE, outs=outs)
+            torch.cuda.synchronize()
+            GH.check_outputs(wl, results, exp)
+    finally:
+        buf.close()
