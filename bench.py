@@ -449,7 +449,8 @@ SWEEP = (("tiny", (16,), "fused"), ("2A2F", (1, 8, 32, 128, 512, 2048), "fused")
 
 def measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=True):
     """Every row of SWEEP, one CUDA graph replay per round trip: mean µs after
-    an L2 flush and back to back, algorithmic bytes, GB/s and the fraction of
+    an L2 flush and back to back (median of three such measurements),
+    algorithmic bytes, GB/s and the fraction of
     the HBM peak (from 512 tokens per source; below, the round trip is bound
     by latency), the pages' cell for the same layout as context, and the
     oracle's time for the same round trip on this host. Single-worker
@@ -467,7 +468,11 @@ def measure_sweep(torch, afd, W, dev, flush, peak, with_oracle=True):
                 variants += [("cached", dict(cached=True)), ("batched collect", dict(batched=True))]
             for label, kw in variants:
                 g = rig.graph(**kw)
-                us, btb = replay_stats(torch, g, flush)
+                # median of three measurements: single replays fall on a ~2 µs grid, and
+                # a back-to-back run settles on one grid step or the next
+                stats = [replay_stats(torch, g, flush) for _ in range(3)]
+                us = statistics.median(x[0] for x in stats)
+                btb = statistics.median(x[1] for x in stats)
                 del g
                 ab = algorithmic_bytes(wl, inp)
                 gbs = ab["total"] / (us * 1e-6) / 1e9
