@@ -71,7 +71,11 @@ constexpr int kErrRange = 5;    // AFD_ERR_ROUTE_RANGE
 constexpr int kErrDup = 6;      // AFD_ERR_ROUTE_DUP
 constexpr int kErrTimeout = 11; // AFD_ERR_TIMEOUT
 constexpr int kDefaultWaitPolls = 1 << 22;  // see afd_set_wait_limit
-constexpr int kBulkRowMax = 8192;  // rows up to this many bytes take the bulk-copy scatter
+// Rows up to this many bytes take the bulk-copy scatter (two row buffers per
+// two-warp block: 33 KB of shared memory at the limit, under the 48 KB a
+// launch gets without opting in). 2A2F round trip at T=2048: H7168 172.1 ->
+// 163.8 us and H8192 196.2 -> 186.5 us against the register scatter.
+constexpr int kBulkRowMax = 16384;
 constexpr unsigned long long kNoError = ~0ull;
 
 // The sticky route error: the smallest key wins, so the reported route is the

@@ -1,9 +1,10 @@
-"""Rows wider than the bulk-copy limit (8 KB): BF16 rows of 14 and 16 KB go
-through the register scatter (16-byte vector copies) and, for a cached
-dispatch, the register cached scatter; FP8 rows of exactly 8 KB are the
-widest the bulk scatter takes. Ragged multi-source batches (one source empty)
-exercise the scatter's source order (last source first). Every result is
-compared with the oracle bit for bit."""
+"""Wide rows: BF16 rows of 14 and 16 KB (16 KB is the widest the bulk-copy
+scatter takes) and FP8 rows of 8 KB go through the bulk scatter with large
+shared-memory buffers; BF16 rows of 32 KB go through the register scatter
+(16-byte vector copies) and, for a cached dispatch, the register cached
+scatter. Ragged multi-source batches (one source empty) exercise the
+scatter's source order (last source first). Every result is compared with
+the oracle bit for bit."""
 import pytest
 import torch
 
@@ -30,6 +31,8 @@ WIDE = [
                T=(512, 77), seed=1202),
     W.Workload("fp8-3A2F-H8192", A=3, F=2, E=64, K=4, H=8192, alpha=16, capacity=1024, bucket=1024,
                T=(257, 640, 0), dtype="fp8", seed=1203),
+    W.Workload("3A2F-H16384", A=3, F=2, E=32, K=4, H=16384, alpha=4, capacity=256, bucket=256,
+               T=(256, 131, 0), seed=1204),
 ]
 
 
