@@ -515,9 +515,10 @@ __device__ __forceinline__ bool drain_phase_warp(uint64_t* mbar, uint32_t parity
 // One bulk copy of `bytes` from shared memory to global memory, with an L2
 // evict-last policy: the rows are read again soon, by the combine (with the
 // identity expert) or by the expert, and kept dirty in L2 they are not
-// written back while the combine streams its replies (round trips after an
-// L2 flush: FP8 2A2F T=2048 51.5 -> 49.5 us, skew 3A:1F 69.4 -> 67.4, H4096
-// 95.8 -> 94.0; 2A2F H2048 48.0 -> 48.1, 49.2 -> 47.5 back to back).
+// written back while the combine streams its replies (round trips at T=2048
+// after an L2 flush that evicts such lines too: FP8 2A2F 51.4 -> 49.7 us,
+// skew 3A:1F 69.6 -> 68.1, H4096 95.6 -> 94.2; 2A2F H2048 48.1 -> 48.6,
+// within the run-to-run spread, and 49.1 -> 47.2 back to back).
 __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
   uint64_t pol;
   asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
