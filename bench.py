@@ -170,6 +170,8 @@ class L2Flush:
     evict-last policy (afd_l2_flush): the scatter writes its rows with that
     policy, and ordinary writes and reads would not evict them."""
 
+    KERNELS = 3  # launches per flush: write, read, discard
+
     def __init__(self, torch, dev):
         self.scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         self.torch = torch
@@ -876,10 +878,11 @@ def main():
             "peak_gbs": peak, "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": (4 * launches_per_step - (wl.A - 1)) * args.steps,
+            "gpu_launches": (4 * launches_per_step - (wl.A - 1) + 6 * L2Flush.KERNELS) * args.steps,
             "gpu_launches_note": "per step: the round-trip graph, the same exchange phase by phase "
-                                 "(one after another, then each after an L2 flush), and the round "
-                                 "trip with one batched collect",
+                                 "(one after another, then each after an L2 flush), the round trip "
+                                 "with one batched collect, and the six L2 flushes between them "
+                                 "(afd_l2_flush: three kernels each, outside every event pair)",
             "back_to_back_us": round(btb_us, 2),
             "eager_us": round(eager_us, 2),
             "collect_all_us": round(batched_us, 2),
