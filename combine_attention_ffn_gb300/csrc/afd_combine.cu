@@ -206,8 +206,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
 
 // ---- two-stage combine (optionally with E4M3 partials) ----
 
-__device__ __forceinline__ float bf16_round(float v) {
-  return __bfloat162float(__float2bfloat16_rn(v));
+// Rounds a and b to BF16 (nearest even) with one paired conversion.
+__device__ __forceinline__ void bf16_round2(float& a, float& b) {
+  const uint32_t u = pack_bf16x2(a, b);
+  a = __uint_as_float(u << 16);
+  b = __uint_as_float(u & 0xffff0000u);
 }
 
 // 2^e as an FP32 value (e in [-126, 127]).
@@ -337,7 +340,7 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
       if ((okmask >> j) & 1u) fma8(part, wk[j], buf[j]);
       if (!((bnd >> j) & 1u)) continue;  // the same for the whole warp
 #pragma unroll
-      for (int e = 0; e < 8; ++e) part[e] = bf16_round(part[e]);
+      for (int e = 0; e < 8; e += 2) bf16_round2(part[e], part[e + 1]);
       if (kMode == AFD_COMBINE_TWO_STAGE_FP8) {
         // one power-of-two scale per 128 elements: 16 lanes x 8 elements
         float amax = 0.0f;
@@ -347,19 +350,22 @@ __device__ __forceinline__ void sum_seg(uint4* out_row, const uint4 (&buf)[kGrou
         for (int d = 1; d < 16; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
         const int ge = group_exponent(amax);
         const float down = exp2_int(-ge), up = exp2_int(ge);
+        // the decoded partial is an FP32 value of its own before the sum
+        // (a group amax of 248 * 2^120 or more decodes to infinity), so the
+        // product and the sum are rounded separately, never fused
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
           float a = part[e] * down, b = part[e + 1] * down;
           e4m3_round_trip2(a, b);
-          part[e] = a * up;
-          part[e + 1] = b * up;
+          acc[e] = __fadd_rn(acc[e], __fmul_rn(a, up));
+          acc[e + 1] = __fadd_rn(acc[e + 1], __fmul_rn(b, up));
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = acc[e] + part[e];
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[e] = acc[e] + part[e];
-        part[e] = 0.0f;
-      }
+      for (int e = 0; e < 8; ++e) part[e] = 0.0f;
     }
   }
   uint4 o;

@@ -113,3 +113,32 @@ def test_two_stage_many_workers(mode, F, T):
         GH.check_outputs(wl, results, exp)
     finally:
         buf.close()
+
+
+@pytest.mark.parametrize("v,want", sorted(TS.TOP_BINADE_CASES.items()))
+def test_two_stage_fp8_top_binade_on_gpu(v, want):
+    """A worker partial in BF16's top binade: from a group amax of 248 * 2^120
+    the decoded partial is infinite (design page, section 19, "Accuracy"), so
+    the sum is too; the oracle's pin gives the same bits."""
+    H = 256
+    buf = afd.Buffer(1, 2, 4, 2, H, 1, 1, "bf16", combine_mode=afd.COMBINE_TWO_STAGE_FP8)
+    try:
+        x = torch.zeros((1, H), dtype=torch.bfloat16, device="cuda")
+        ids = torch.tensor([[0, 2]], dtype=torch.int64, device="cuda")
+        w = torch.ones((1, 2), dtype=torch.float32, device="cuda")
+        buf.source_dispatch(0, x, ids, w, bucket=1)
+        recvs = [buf.worker_receive(f, bucket=1) for f in range(2)]
+        replies = []
+        for f in range(2):
+            rep = torch.zeros((recvs[f].num_rows, H), dtype=torch.int32)
+            for row, src in enumerate(recvs[f].row_src.cpu().tolist()):
+                if src >= 0:
+                    rep[row] = TS.TOP_BINADE_OTHER if src % 2 == 0 else v
+            replies.append(rep.to(torch.int16).cuda().view(torch.bfloat16))
+            buf.worker_reply(f, replies[f], recvs[f].receipt)
+        out = buf.source_collect(0, num_tokens=1)
+        torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.all(got == want), (hex(v), hex(int(got[0, 0])))
+    finally:
+        buf.close()

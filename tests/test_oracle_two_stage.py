@@ -214,3 +214,38 @@ def test_two_stage_crafted_order():
     fused = oracle.combine(p, ids, w, d["slot"], r_stride, reply)
     assert np.all(two[0, 0] == 0x3F81)
     assert np.all(fused[0, 0] == 0x3F80)
+
+
+# Worker 0's partial is -1.5 * 2^127 (BF16 0xFF40, exact in E4M3 with scale
+# 2^119); worker 1's partial is v. The design page (section 19, "Accuracy")
+# says a group amax of 248 * 2^120 or more decodes to infinity (the top BF16
+# binade is not representable): with scale 2^120, 248 is the tie between the
+# E4M3 values 240 and 256 and goes to the even code, 256, and 256 * 2^120 is
+# beyond the FP32 range. Below it the partial decodes to 240 * 2^120.
+#   v >= 248 * 2^120: -1.5 * 2^127 + inf = inf                  -> 0x7F80
+#   v in (232, 248) * 2^120: -1.5 * 2^127 + 1.875 * 2^127 = 1.5 * 2^125 -> 0x7E40
+# Decoding exactly and rounding only the sum (2^128 - 1.5 * 2^127 = 2^126,
+# 0x7E80) is the reading this rules out.
+TOP_BINADE_CASES = {0x7F78: 0x7F80, 0x7F7F: 0x7F80, 0x7F76: 0x7E40, 0x7F70: 0x7E40}
+TOP_BINADE_OTHER = 0xFF40
+
+
+def test_two_stage_fp8_top_binade_decodes_to_infinity():
+    H = 128
+    ids = np.array([[[0, 2]]], np.int64)  # experts 0 and 2: workers 0 and 1
+    w = np.ones((1, 1, 2), np.float32)
+    p = oracle.Problem(1, 2, 4, 2, H, 1, 1, oracle.BF16, [1])
+    lay = oracle.layout(p, ids)
+    r_stride = int(lay["r_exact"].max())
+    d = oracle.dispatch(p, ids, w, np.zeros((1, 1, H), np.uint16), None, lay, r_stride)
+    for v, want in TOP_BINADE_CASES.items():
+        reply = np.zeros((2, r_stride, H), np.uint16)
+        reply[0, d["slot"][0, 0, 0], :] = TOP_BINADE_OTHER
+        reply[1, d["slot"][0, 0, 1], :] = v
+        out = oracle.combine_two_stage(p, ids, w, d["slot"], r_stride, reply, fp8=True)
+        assert np.all(out[0, 0] == want), (hex(v), hex(int(out[0, 0, 0])))
+        # with BF16 partials nothing overflows: (v - 1.5 * 2^127) rounded to BF16
+        two = oracle.combine_two_stage(p, ids, w, d["slot"], r_stride, reply, fp8=False)
+        vf = float(np.uint32(v << 16).view(np.float32))
+        exp_bf16 = exact.bf16_bits(exact.round_bf16(Fraction(vf) - Fraction(3, 2) * Fraction(2) ** 127))
+        assert np.all(two[0, 0] == exp_bf16)
