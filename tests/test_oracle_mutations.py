@@ -61,6 +61,8 @@ MUTATIONS = {
     "partial_not_rounded": ("part[h] = orc_bf16_to_float(orc_float_to_bf16(a));", "part[h] = a;"),
     "worker_order_first_route": ("for (int j = k + 1; j < p->K; ++j) {\n          int64_t rj = route_index(p, s, t, j);\n          if (slot[rj] >= 0 && (int)(ids[rj] / Ef) == f) last = 0;",
                                  "for (int j = 0; j < k; ++j) {\n          int64_t rj = route_index(p, s, t, j);\n          if (slot[rj] >= 0 && (int)(ids[rj] / Ef) == f) last = 0;"),
+    "fp8_decode_clamped": ("part[h] = ldexpf(orc_e4m3_to_float(q), e);",
+                           "part[h] = fminf(fmaxf(ldexpf(orc_e4m3_to_float(q), e), -3.4028235e38f), 3.4028235e38f);"),
     "fp8_dequant_wrong_scale": ("part[h] = ldexpf(orc_e4m3_to_float(q), e);", "part[h] = ldexpf(orc_e4m3_to_float(q), e + 1);"),
     "dispatch_worker_modulo": ("int f = (int)(e / Ef);", "int f = (int)(e % p->F);"),
     "combine_worker_modulo": ("int f = (int)(ids[ri] / Ef);\n          float r",
@@ -214,6 +216,12 @@ def _pins(orc, report=None) -> list:
             want = TS._two_stage_exact(ids, w, r["slot"], r["reply"], E // F, [2], fp8)
             assert np.array_equal(r["out"], want)
 
+    def two_stage_top_binade():
+        import test_oracle_two_stage as TS
+        got = TS.top_binade_outputs(orc)
+        for v, want in TS.TOP_BINADE_CASES.items():
+            assert got[v][0] == want
+
     def fp8_formats():
         import test_oracle_two_stage as TS
         f32 = np.float32
@@ -224,7 +232,8 @@ def _pins(orc, report=None) -> list:
         assert orc.float_to_e4m3(x).tolist() == [0x00, 0x02, 0x7E, 0x7E, 0x3A, 0x38]
 
     for name, fn in [("golden_layout", golden_layout), ("random_layout_dispatch", random_layout_and_dispatch),
-                     ("two_stage", two_stage), ("fp8_formats", fp8_formats),
+                     ("two_stage", two_stage), ("two_stage_top_binade", two_stage_top_binade),
+                     ("fp8_formats", fp8_formats),
                      ("fp8", fp8_dispatch_and_expert), ("validate", validate_rules),
                      ("combine_exact", combine_exact), ("combine_crafted", combine_crafted),
                      ("bf16", bf16_vs_torch), ("e4m3", e4m3_vs_torch)]:

@@ -230,22 +230,34 @@ TOP_BINADE_CASES = {0x7F78: 0x7F80, 0x7F7F: 0x7F80, 0x7F76: 0x7E40, 0x7F70: 0x7E
 TOP_BINADE_OTHER = 0xFF40
 
 
-def test_two_stage_fp8_top_binade_decodes_to_infinity():
+def top_binade_outputs(orc=None):
+    """{v: (FP8-partials output word, BF16-partials output word)} for the
+    top-binade token above, as the oracle computes them."""
     H = 128
     ids = np.array([[[0, 2]]], np.int64)  # experts 0 and 2: workers 0 and 1
     w = np.ones((1, 1, 2), np.float32)
     p = oracle.Problem(1, 2, 4, 2, H, 1, 1, oracle.BF16, [1])
-    lay = oracle.layout(p, ids)
+    lay = oracle.layout(p, ids, orc)
     r_stride = int(lay["r_exact"].max())
-    d = oracle.dispatch(p, ids, w, np.zeros((1, 1, H), np.uint16), None, lay, r_stride)
-    for v, want in TOP_BINADE_CASES.items():
+    d = oracle.dispatch(p, ids, w, np.zeros((1, 1, H), np.uint16), None, lay, r_stride, orc)
+    res = {}
+    for v in TOP_BINADE_CASES:
         reply = np.zeros((2, r_stride, H), np.uint16)
         reply[0, d["slot"][0, 0, 0], :] = TOP_BINADE_OTHER
         reply[1, d["slot"][0, 0, 1], :] = v
-        out = oracle.combine_two_stage(p, ids, w, d["slot"], r_stride, reply, fp8=True)
-        assert np.all(out[0, 0] == want), (hex(v), hex(int(out[0, 0, 0])))
+        words = []
+        for fp8 in (True, False):
+            out = oracle.combine_two_stage(p, ids, w, d["slot"], r_stride, reply, fp8, orc)
+            assert np.all(out[0, 0] == out[0, 0, 0])
+            words.append(int(out[0, 0, 0]))
+        res[v] = tuple(words)
+    return res
+
+
+def test_two_stage_fp8_top_binade_decodes_to_infinity():
+    got = top_binade_outputs()
+    for v, want in TOP_BINADE_CASES.items():
+        assert got[v][0] == want, (hex(v), hex(got[v][0]))
         # with BF16 partials nothing overflows: (v - 1.5 * 2^127) rounded to BF16
-        two = oracle.combine_two_stage(p, ids, w, d["slot"], r_stride, reply, fp8=False)
         vf = float(np.uint32(v << 16).view(np.float32))
-        exp_bf16 = exact.bf16_bits(exact.round_bf16(Fraction(vf) - Fraction(3, 2) * Fraction(2) ** 127))
-        assert np.all(two[0, 0] == exp_bf16)
+        assert got[v][1] == exact.bf16_bits(exact.round_bf16(Fraction(vf) - Fraction(3, 2) * Fraction(2) ** 127))
