@@ -96,7 +96,8 @@ enum { AFD_BF16 = 0, AFD_FP8_E4M3 = 1 };
  * TWO_STAGE_FP8: as TWO_STAGE, with each partial carried as E4M3 values and
  *   a shared power-of-two factor 2^e for every block of 128 of them (e the
  *   smallest integer >= -117 with amax <= 448 * 2^e): the lossy reply format
- *   of section 19.
+ *   of section 19. Each decoded value q * 2^e is rounded to FP32 before it is
+ *   added, so a block whose amax is 248 * 2^120 or more decodes to infinity.
  * The two-stage modes need top_k <= 8. */
 enum { AFD_COMBINE_FUSED = 0, AFD_COMBINE_TWO_STAGE = 1, AFD_COMBINE_TWO_STAGE_FP8 = 2 };
 
