@@ -62,41 +62,52 @@ int g_seg2_blocks_per_sm = 0;
 // receipts: L2-only loads.
 //
 // A combine launched right after the previous combine of the same exchange
-// on the same stream (p.early) needs no dependency wait to start: its launch
-// implies that every block of that combine has passed its own wait (it lets
-// dependents launch only after it), so the scatter, the expert and
+// on the same stream (p.early != 0) needs no dependency wait to start: its
+// launch implies that every block of that combine has passed its own wait
+// (it lets dependents launch only after it), so the scatter, the expert and
 // everything before them have completed, and the replies stay unchanged for
 // this kernel's whole lifetime, which is what non-coherent loads require. It
 // waits at its end instead, so that it completes only after its predecessor
 // (what comes after it in the stream may rely on the whole exchange being
 // done). Any other combine waits first and then lets dependents launch.
-__device__ __forceinline__ uint4 ld_reply(const uint4* p, bool early) {
-#if AFD_EARLY_LOADS == 1
-  if (early) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-  }
-#endif
-  (void)early;
-  return ld_once(p);
+// An early start takes one of two forms (kEarlyFence, kEarlyL2):
+//  * kEarlyFence: a device-scope acquire fence first, so that no line an
+//    earlier kernel left in this SM's L1 is used, then the streaming loads;
+//  * kEarlyL2 (launches of fewer tokens than the per-token kernel takes):
+//    every reply and receipt load reads L2 only, which holds the completed
+//    writes, so no fence is needed; at these sizes L2-only loads cost no
+//    more than the streaming ones, while the fence costs 0.45 us.
+constexpr int kEarlyFence = 1, kEarlyL2 = 2;
+
+__device__ __forceinline__ uint4 ld_l2(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
+
 
 // combine_kernel's reply loads: the same streaming loads with an L2
 // evict-first policy (replies are read once). Measured with few tokens per
 // launch: 2A2F round trip back to back T=1 10.3 -> 8.4 us, T=32 12.3 -> 10.9,
 // T=512 22.6 -> 20.5 (evict_normal or evict_last policies measure the same;
 // the per-token kernel, which streams far more bytes, and the segmented
-// two-stage kernel are slower with them).
+// two-stage kernel are slower with them). kL2: L2-only loads with the same
+// policy (the instantiation launched for an early start of kind kEarlyL2).
+template <bool kL2>
 __device__ __forceinline__ uint4 ld_reply_seg(const uint4* p) {
   uint64_t pol;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(pol));
+  if (kL2)
+    asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+  else
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
   return v;
 }
 
@@ -104,7 +115,7 @@ __device__ __forceinline__ void combine_begin(const CombineParams& p) {
   AFD_STAMP(g_combine_stamps, p.early ? 1 : 0, 0);
   if (!p.early) {
     pdl_wait();
-  } else {
+  } else if (p.early == kEarlyFence) {
 #if AFD_EARLY_FENCE
     // a device-scope acquire before the first load: no line an earlier
     // kernel left in this SM's L1 is used
@@ -140,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int U>
+template <int U, bool kL2>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
   combine_begin(p);  // receipts and replies come from earlier kernels
   const int lane = threadIdx.x & 31;
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
           const uint4* row = reinterpret_cast<const uint4*>(
               p.reply[c >> kWorkerShift] + (int64_t)(c & kRowMask) * p.H);
 #pragma unroll
-          for (int u = 0; u < U; ++u) buf[j][u] = ld_reply_seg(row + v0 + u * 32);
+          for (int u = 0; u < U; ++u) buf[j][u] = ld_reply_seg<kL2>(row + v0 + u * 32);
         }
       }
 #pragma unroll
@@ -305,11 +316,17 @@ __device__ __forceinline__ uint32_t token_routes_grouped(const CombineParams& p,
   return okmask;
 }
 
+// kL2: L2-only loads (an early start of kind kEarlyL2; segmented launches
+// only), else the streaming loads.
+template <bool kL2>
 __device__ __forceinline__ void load_seg(uint4 (&buf)[kGroup], const uint16_t* const (&rowp)[kGroup],
-                                         uint32_t okmask, int v, bool early) {
+                                         uint32_t okmask, int v) {
 #pragma unroll
   for (int j = 0; j < kGroup; ++j)
-    if ((okmask >> j) & 1u) buf[j] = ld_reply(reinterpret_cast<const uint4*>(rowp[j]) + v, early);
+    if ((okmask >> j) & 1u) {
+      const uint4* a = reinterpret_cast<const uint4*>(rowp[j]) + v;
+      buf[j] = kL2 ? ld_l2(a) : ld_once(a);
+    }
 }
 
 // Sums one segment (this lane's 8 elements of every route) and stores it.
@@ -408,12 +425,12 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED               ?
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) rowp[j] += seg0 * 256;
     uint4 a[kGroup], b[kGroup];
-    load_seg(a, rowp, okmask, lane, p.early);
+    load_seg<false>(a, rowp, okmask, lane);
     int seg = 0;
     for (; seg + 2 <= nseg; seg += 2) {
-      load_seg(b, rowp, okmask, (seg + 1) * 32 + lane, p.early);
+      load_seg<false>(b, rowp, okmask, (seg + 1) * 32 + lane);
       sum_seg<kMode>(out_row, a, wk, bnd, okmask, seg * 32 + lane);
-      if (seg + 2 < nseg) load_seg(a, rowp, okmask, (seg + 2) * 32 + lane, p.early);
+      if (seg + 2 < nseg) load_seg<false>(a, rowp, okmask, (seg + 2) * 32 + lane);
       sum_seg<kMode>(out_row, b, wk, bnd, okmask, (seg + 1) * 32 + lane);
     }
     if (seg < nseg) sum_seg<kMode>(out_row, a, wk, bnd, okmask, seg * 32 + lane);
@@ -423,7 +440,7 @@ __global__ void __launch_bounds__(64, kMode == AFD_COMBINE_FUSED               ?
 
 // Few tokens: a warp per (token, 512-byte segment), as combine_kernel<1>,
 // with the two-stage rule.
-template <int kMode>
+template <int kMode, bool kL2>
 __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_constant__ CombineParams p) {
   combine_begin(p);
   const int lane = threadIdx.x & 31;
@@ -446,7 +463,7 @@ __global__ void __launch_bounds__(256) combine_two_stage_kernel(const __grid_con
     const uint32_t okmask = kMode == AFD_COMBINE_FUSED ? token_routes(p, r, rowp, wk)
                                                        : token_routes_grouped(p, r, rowp, wk, bnd);
     uint4 buf[kGroup];
-    load_seg(buf, rowp, okmask, seg * 32 + lane, p.early);
+    load_seg<kL2>(buf, rowp, okmask, seg * 32 + lane);
     sum_seg<kMode>(reinterpret_cast<uint4*>(p.out[s] + (int64_t)t * p.out_stride[s]), buf, wk, bnd,
                    okmask, seg * 32 + lane);
   }
@@ -471,9 +488,12 @@ cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, cudaStream_t stre
 
 // Both kernels start as programmatic dependents of the previous kernel on the
 // stream and wait for it before reading anything.
-cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stream) {
-  if (p.total_tokens <= 0) return cudaSuccess;
-  if (p.K <= kGroup && p.total_tokens >= sm_cap * AFD_TOKEN_COMBINE_MIN) {
+cudaError_t launch_combine(const CombineParams& p_in, int sm_cap, cudaStream_t stream) {
+  if (p_in.total_tokens <= 0) return cudaSuccess;
+  CombineParams p = p_in;
+  const bool small = p.total_tokens < sm_cap * AFD_TOKEN_COMBINE_MIN;
+  if (p.early) p.early = small ? kEarlyL2 : kEarlyFence;
+  if (p.K <= kGroup && !small) {
     // enough tokens for a warp each on every SM: the pipelined per-token
     // kernel, in two-warp blocks so that tokens spread evenly over the SMs
     int64_t grid = ((int64_t)p.total_tokens * AFD_COMBINE_SPLIT + 1) / 2;
@@ -485,13 +505,16 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
       default: return launch_pdl(combine_token_kernel<AFD_COMBINE_FUSED>, grid, 64, stream, p);
     }
   }
+  const bool l2 = p.early == kEarlyL2;
   if (p.mode != AFD_COMBINE_FUSED) {
     const int64_t items = (int64_t)p.total_tokens * (p.H >> 8);
     int64_t grid = (items + 7) / 8;
     if (grid > (int64_t)sm_cap * 8) grid = (int64_t)sm_cap * 8;
-    return p.mode == AFD_COMBINE_TWO_STAGE_FP8
-               ? launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>, grid, 256, stream, p)
-               : launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>, grid, 256, stream, p);
+    if (p.mode == AFD_COMBINE_TWO_STAGE_FP8)
+      return l2 ? launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8, true>, grid, 256, stream, p)
+                : launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8, false>, grid, 256, stream, p);
+    return l2 ? launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE, true>, grid, 256, stream, p)
+              : launch_pdl(combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE, false>, grid, 256, stream, p);
   }
   const int64_t slices = (int64_t)p.total_tokens * (p.H >> 8);
   // Two slices per item when one slice per warp would need more warps than
@@ -512,15 +535,19 @@ cudaError_t launch_combine(const CombineParams& p, int sm_cap, cudaStream_t stre
       const int64_t need2 = (slices / 2 + 7) / 8;
       if (grid > need2) grid = need2;
       if (grid < 1) grid = 1;
-      return launch_pdl(combine_kernel<2>, grid, 256, stream, p);
+      return l2 ? launch_pdl(combine_kernel<2, true>, grid, 256, stream, p)
+                : launch_pdl(combine_kernel<2, false>, grid, 256, stream, p);
     }
   }
   const int64_t cap = (int64_t)sm_cap * 8;  // blocks of 8 warps
   const int64_t items = wide ? slices / 2 : slices;
   int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;
-  return wide ? launch_pdl(combine_kernel<2>, grid, 256, stream, p)
-              : launch_pdl(combine_kernel<1>, grid, 256, stream, p);
+  if (wide)
+    return l2 ? launch_pdl(combine_kernel<2, true>, grid, 256, stream, p)
+              : launch_pdl(combine_kernel<2, false>, grid, 256, stream, p);
+  return l2 ? launch_pdl(combine_kernel<1, true>, grid, 256, stream, p)
+            : launch_pdl(combine_kernel<1, false>, grid, 256, stream, p);
 }
 
 cudaError_t configure_combine_kernels() {
@@ -528,13 +555,16 @@ cudaError_t configure_combine_kernels() {
   for (const void* k : {(const void*)combine_token_kernel<AFD_COMBINE_FUSED>,
                         (const void*)combine_token_kernel<AFD_COMBINE_TWO_STAGE>,
                         (const void*)combine_token_kernel<AFD_COMBINE_TWO_STAGE_FP8>,
-                        (const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
-                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE>,
-                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8>})
+                        (const void*)combine_kernel<1, false>, (const void*)combine_kernel<2, false>,
+                        (const void*)combine_kernel<1, true>, (const void*)combine_kernel<2, true>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE, false>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8, false>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE, true>,
+                        (const void*)combine_two_stage_kernel<AFD_COMBINE_TWO_STAGE_FP8, true>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kSharedCarveout);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg1_blocks_per_sm, combine_kernel<1>, 256, 0);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg2_blocks_per_sm, combine_kernel<2>, 256, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg1_blocks_per_sm, combine_kernel<1, false>, 256, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_seg2_blocks_per_sm, combine_kernel<2, false>, 256, 0);
   return e;
 }
 

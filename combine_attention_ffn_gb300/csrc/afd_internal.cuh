@@ -42,11 +42,8 @@ constexpr int kSmallSmemMax = 110 * 1024;
 #ifndef AFD_TWO_STAGE_FP8_BLOCKS
 #define AFD_TWO_STAGE_FP8_BLOCKS 8  // the same, with E4M3 partials
 #endif
-#ifndef AFD_EARLY_LOADS
-#define AFD_EARLY_LOADS 0         // 1: an early-started combine reads replies with ld.global.cg (L2 only)
-#endif
 #ifndef AFD_EARLY_FENCE
-#define AFD_EARLY_FENCE 1         // an early-started combine begins with a device-scope acquire fence
+#define AFD_EARLY_FENCE 1         // an early-started per-token combine begins with a device-scope acquire fence
 #endif
 #ifndef AFD_COMBINE_EARLY
 #define AFD_COMBINE_EARLY 1       // a combine right after another one of the same exchange starts at once
@@ -130,8 +127,9 @@ struct CombineParams {
   const uint16_t* reply[kMaxWorkers];// BF16 [rows][H] per worker
   int32_t A, K, H, total_tokens;
   int32_t mode;                      // AFD_COMBINE_*
-  int32_t early;                     // 1: the previous kernel on the stream is a combine of the
-                                     // same exchange (start at once, wait for it at the end)
+  int32_t early;                     // nonzero: the previous kernel on the stream is a combine of
+                                     // the same exchange (start at once, wait for it at the end;
+                                     // launch_combine picks the form, afd_combine.cu)
   int32_t share;                     // combines of this exchange expected to run side by side
                                      // (one per source when each source collects on its own)
 };

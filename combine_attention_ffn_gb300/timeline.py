@@ -23,7 +23,7 @@ POINTS = {
     "scatter": ("start", "wait passed", "first row in shared memory", "stores issued",
                 "stores complete", "end"),
     "combine": ("start", "wait passed", "sums stored", "end"),
-    "combine-early": ("start", "fence done", "sums stored", "end (after its wait)"),
+    "combine-early": ("start", "ready to load", "sums stored", "end (after its wait)"),
 }
 
 
