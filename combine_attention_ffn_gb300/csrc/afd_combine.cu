@@ -76,7 +76,7 @@ int g_seg2_blocks_per_sm = 0;
 //  * kEarlyL2 (launches of fewer tokens than the per-token kernel takes):
 //    every reply and receipt load reads L2 only, which holds the completed
 //    writes, so no fence is needed; at these sizes L2-only loads cost no
-//    more than the streaming ones, while the fence costs 0.45 us.
+//    more than the streaming ones.
 constexpr int kEarlyFence = 1, kEarlyL2 = 2;
 
 __device__ __forceinline__ uint4 ld_l2(const uint4* p) {
