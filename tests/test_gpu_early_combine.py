@@ -41,9 +41,12 @@ def _touch_through_l1(recvs):
 
 
 @pytest.mark.parametrize("name,T", [("2A2F", 2048), ("2A2F", 64), ("2A2F-H4096", 700),
-                                    ("fp8-2A2F", 300)])
+                                    ("fp8-2A2F", 300),
+                                    # a large launch then a small early one (L2-only loads, no
+                                    # fence), and a small launch then a large early one (fence)
+                                    ("2A2F", (2048, 100)), ("2A2F", (100, 2048))])
 def test_early_combine_sees_every_new_reply(name, T):
-    wl = W.named(name, T=T)
+    wl = W.named(name, T=T) if isinstance(T, int) else W.named(name).with_tokens(T)
     mode = GH.IDENTITY if wl.dtype == "bf16" else GH.SCALE
     buf = GH.make_buffer(wl)
     try:
