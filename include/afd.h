@@ -325,7 +325,7 @@ AFD_API afd_status afd_l2_flush(void* scratch, int64_t bytes, afd_stream stream)
  * and 7), 1 the scatter (0 start, 1 wait passed, 2 first row in shared
  * memory, 3 all stores issued, 4 stores complete, 5 end), 2 a combine that
  * waits first and 3 an early-started combine (0 start, 1 wait passed or
- * fence done, 2 sums stored, 3 end). The stamps are global to the process;
+ * ready to load, 2 sums stored, 3 end). The stamps are global to the process;
  * the last launch of a kind overwrites the earlier ones; blocks past 4096
  * are not recorded.
  *   host   host uint64 array of `count` >= 131072 elements
